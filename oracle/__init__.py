@@ -1,0 +1,27 @@
+"""CPU oracle of the single-GPU Mixture-of-Experts layer forward.
+
+TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the benchmark's CPU
+baseline leg import this package; the product path (the CUDA library and its
+Python binding) never does, and shares no code with it.  It is plain numpy in
+float64, slow and written to be checked by eye against the method's
+definition.
+
+Parity unpinned: ``traffic_model_bytes`` (the fused/unfused byte model; the
+35 % figure the review quotes does not follow from the byte counts it prints).
+"""
+from .moe_oracle import (  # noqa: F401
+    Routing,
+    widen,
+    router_logits,
+    router_scores,
+    select_experts,
+    selection_margin,
+    routing_weights,
+    permute,
+    swiglu_expert,
+    combine,
+    forward,
+    forward_tokens,
+    dense_masked_forward,
+    traffic_model_bytes,
+)
