@@ -1,0 +1,440 @@
+"""Benchmark of the single-GPU MoE layer forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--T T] [--alpha A]
+                    [--impl ours|reference] [--no-sweep] [--no-cpu]
+
+One step = one moe_forward_ex over one batch of T tokens (router + top-k,
+permute, fused gate+up GEMM, down GEMM, combine), inputs and weights already
+resident in HBM.  Prints ONE JSON line.  The default workload is the
+Mixtral-8x7B-shaped layer (H=4096, F=14336, E=8, top-2) at T=4096; the
+other token counts of that layer (1, 32, 128, 512) are timed in the same run
+and reported under "sweep".
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the layer forward has no exchange step); the time is the max over ranks and
+the value the tokens of all ranks divided by it.
+
+--impl reference times the CPU oracle (float64 numpy) on the host cores on
+bounded samples of the same workload and prints the same line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from synth.workloads import T_SWEEP  # noqa: E402
+
+METRIC = "MoE layer fwd tokens/s on 1 GB300; % of max(HBM, bf16 tensor) roofline"
+NOMINAL_HBM = 8.0e12       # B/s, the layer roofline's denominators
+NOMINAL_BF16 = 2.25e15     # FLOP/s
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+STAGES = ("route", "permute", "gate_up_gemm", "down_gemm", "combine")
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_cfg(moe, wl, d):
+    return moe.MoeConfig.make(score=wl.score, renormalize=wl.renormalize, route_scale=wl.route_scale,
+                              n_group=wl.n_group, topk_group=wl.topk_group, group_topn=wl.group_topn,
+                              logit_bias=d.get("logit_bias"), ws_gate=d.get("ws_gate"), ws_up=d.get("ws_up"),
+                              ws_down=d.get("ws_down"), w_shared_gate=d.get("w_shared_gate"))
+
+
+def launches_per_forward(wl) -> int:
+    # router+top-k, [shared gate], bitmap, scan, gather, gate+up GEMM, down GEMM, combine
+    return 7 + (1 if wl.shared_gate else 0)
+
+
+def stage_algorithmic(wl, active: int):
+    """Algorithmic FLOPs and bytes of each stage of one forward: what the
+    stage must compute and move at minimum given its inputs and outputs."""
+    T, H, F, E, k = wl.T, wl.H, wl.F, wl.E, wl.k
+    Tk = T * k
+    out = {
+        "route": (2.0 * T * H * E, T * H * 2.0 + E * H * 2.0 + Tk * 8.0),
+        "permute": (0.0, T * H * 2.0 + Tk * H * 2.0 + Tk * 12.0),
+        "gate_up_gemm": (Tk * 4.0 * H * F, active * 4.0 * H * F + Tk * H * 2.0 + Tk * F * 2.0),
+        "down_gemm": (Tk * 2.0 * H * F, active * 2.0 * H * F + Tk * F * 2.0 + Tk * H * 4.0),
+        "combine": (0.0, Tk * H * 4.0 + T * H * 2.0 + Tk * 8.0),
+    }
+    if wl.F_shared:
+        Fs = wl.F_shared
+        f, b = out["gate_up_gemm"]
+        out["gate_up_gemm"] = (f + T * 4.0 * H * Fs, b + 4.0 * H * Fs + T * H * 2.0 + T * Fs * 2.0)
+        f, b = out["down_gemm"]
+        out["down_gemm"] = (f + T * 2.0 * H * Fs, b + 2.0 * H * Fs + T * Fs * 2.0 + T * H * 4.0)
+        f, b = out["combine"]
+        out["combine"] = (f, b + T * H * 4.0)
+    return out
+
+
+def sources_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mixture_experts_layer_06_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources and this workload; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel, {})
+    if e.get("sources_sha") == sources_sha() and e.get("workload") == workload:
+        return e.get("dram_bytes_per_launch")
+    return None
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import mixture_experts_layer_06_gb300 as moe
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("gloo", init_method="env://")
+    torch.cuda.set_device(local)
+    moe.load_library()
+    stream = torch.cuda.current_stream()
+
+    kw = {} if args.alpha is None else {"alpha": args.alpha}
+    T_main = args.T if args.T is not None else max(T_SWEEP[args.workload])
+    sweep_T = [] if args.no_sweep else [t for t in T_SWEEP[args.workload] if t != T_main]
+    T_all = max([T_main] + sweep_T)
+    wl_all = synth.workload(args.workload, T=T_all, **kw)
+    inp = synth.make_inputs(wl_all)
+    d = {}
+    for name, a in inp.items():
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+        d[name] = t.cuda().view(torch.bfloat16) if a.dtype == np.uint16 else t.cuda()
+    cfg = make_cfg(moe, wl_all, d)
+    weight_bytes_per_expert = 6.0 * wl_all.H * wl_all.F
+
+    def run_T(T, K, W, timed_stages):
+        wl = wl_all.with_T(T)
+        x = d["x"][:T]
+        out = torch.empty((T, wl.H), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(moe.moe_workspace_bytes(cfg, T, wl.H, wl.F, wl.E, wl.k), dtype=torch.uint8, device="cuda")
+
+        def fwd():
+            moe.moe_forward_ex(x, d["w_router"], d["w_gate"], d["w_up"], d["w_down"], wl.k, cfg, out=out,
+                               workspace=ws)
+
+        for _ in range(W):
+            fwd()
+        st, raw = moe.moe_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error {moe.moe_status_string(st)} {raw:#x}")
+        # active experts of this batch (for the compulsory-byte roofline)
+        idx, _, _ = moe.moe_route(x, d["w_router"], wl.k, cfg)
+        active = int(torch.unique(idx).numel())
+        ev = None
+        if timed_stages:
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(K):
+            if ev is not None:
+                moe.moe_set_trace_events(ev[i])
+            fwd()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        moe.moe_set_trace_events(None)
+        if world > 1:
+            dist.barrier()
+        ms = start.elapsed_time(stop)
+        res = {"T": T, "ms_total": ms, "active_experts": active, "wl": wl}
+        if ev is not None:
+            per = np.array([[ev[i][j].elapsed_time(ev[i][j + 1]) for j in range(5)] for i in range(K)])
+            res["stage_ms"] = dict(zip(STAGES, per.mean(axis=0).tolist()))
+        st, raw = moe.moe_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error {moe.moe_status_string(st)} {raw:#x}")
+        return res
+
+    pk, pk_kind = peaks()
+    with ClockSampler(local) as clocks:
+        main = run_T(T_main, args.steps, args.warmup, True)
+    clk = clocks.summary()
+
+    ms_main = main["ms_total"]
+    if world > 1:
+        t = torch.tensor([ms_main], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_main = float(t.item())
+    wl = main["wl"]
+    ms_step = ms_main / args.steps
+    value = world * T_main * args.steps / (ms_main / 1e3)
+
+    # layer roofline (nominal denominators) for this batch
+    flops = wl.flops()
+    cbytes = wl.compulsory_bytes(main["active_experts"])
+    t_roof = max(flops / NOMINAL_BF16, cbytes / NOMINAL_HBM)
+
+    # dominant kernel roofline (measured peaks)
+    stage_ms = main["stage_ms"]
+    alg = stage_algorithmic(wl, main["active_experts"])
+    dom = max(stage_ms, key=stage_ms.get)
+    f_dom, b_dom = alg[dom]
+    sec = stage_ms[dom] / 1e3
+    intensity = f_dom / b_dom
+    ridge = pk["bf16_tflops_sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if intensity >= ridge:
+        roof = {"bound": "tensor", "achieved": f_dom / sec / 1e12, "peak": pk["bf16_tflops_sustained"],
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": b_dom / sec / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_source"] = f"{pk_kind} ({'sustained bf16 matmul' if roof['bound'] == 'tensor' else 'copy'})"
+    roof["kernel"] = dom
+    roof["traffic"] = recorded_traffic(dom, wl.label)
+    roof["algorithmic"] = {"flops_per_launch": f_dom, "bytes_per_launch": b_dom}
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(moe, torch, d, cfg, wl, args, stream)
+
+    sweep = []
+    for T in sweep_T:
+        K = max(args.steps, 20) if T <= 32 else args.steps
+        r = run_T(T, K, args.warmup, False)
+        w = r["wl"]
+        ms = r["ms_total"] / K
+        tr = max(w.flops() / NOMINAL_BF16, w.compulsory_bytes(r["active_experts"]) / NOMINAL_HBM)
+        sweep.append({"T": T, "tokens_per_s": T / (ms / 1e3), "us_per_step": ms * 1e3,
+                      "layer_roofline_frac": tr / (ms / 1e3), "active_experts": r["active_experts"]})
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) x, N(0,0.02) weights, bf16)",
+        "config": {"workload": wl.label, "T": wl.T, "H": wl.H, "F": wl.F, "E": wl.E, "k": wl.k,
+                   "routing": f"{wl.score}, renormalize={wl.renormalize}, scale={wl.route_scale}",
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"no flush: the {cbytes / 1e9:.2f} GB of compulsory weight traffic per step exceeds "
+                         f"the 126 MB L2"},
+        "layer_roofline": {"t_roofline_us": t_roof * 1e6, "frac": t_roof / (ms_step / 1e3),
+                           "flops": flops, "compulsory_bytes": cbytes, "active_experts": main["active_experts"],
+                           "denominators": "nominal 8 TB/s HBM, 2.25 PFLOP/s dense bf16"},
+        "roofline": roof,
+        "stages_ms": stage_ms,
+        "e2e": e2e,
+        "clocks": clk,
+        "gpu_launches": launches_per_forward(wl) * args.steps,
+        "sweep": sweep,
+    }
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(wl, inp, budget_s=args.cpu_seconds)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(moe, torch, d, cfg, wl, args, stream):
+    """Same metric through the C ABI with host buffers: per step, copy x in
+    from pinned host memory, run the layer, copy the output back."""
+    T, H = wl.T, wl.H
+    x_host = d["x"][:T].cpu().pin_memory()
+    out_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(d["x"][:T])
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(moe.moe_workspace_bytes(cfg, T, H, wl.F, wl.E, wl.k), dtype=torch.uint8, device="cuda")
+
+    def step():
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_forward_ex(x_dev, d["w_router"], d["w_gate"], d["w_up"], d["w_down"], wl.k, cfg, out=out,
+                           workspace=ws)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    nbytes = T * H * 2
+    return {"value": T * args.steps / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": nbytes,
+            "d2h_bytes_per_step": nbytes, "ms_per_step": ms / args.steps}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def cpu_baseline(wl, inp, budget_s=15.0, sample_tokens=4):
+    """The oracle, as it stands, on the host cores: forward_tokens over
+    consecutive samples of the batch until about budget_s seconds pass."""
+    import oracle
+
+    t0 = time.perf_counter()
+    done = 0
+    start = 0
+    while time.perf_counter() - t0 < budget_s and done < wl.T:
+        toks = np.arange(start, min(start + sample_tokens, wl.T))
+        oracle.forward_tokens(inp, wl, toks)
+        done += toks.size
+        start += toks.size
+    el = time.perf_counter() - t0
+    return {"value": done / el, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{done} tokens of the T={wl.T} batch in groups of {sample_tokens} "
+                      f"(float64 numpy, OpenBLAS threads for the matmuls), {el:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    kw = {} if args.alpha is None else {"alpha": args.alpha}
+    T = args.T if args.T is not None else max(T_SWEEP[args.workload])
+    wl = synth.workload(args.workload, T=T, **kw)
+    inp = synth.make_inputs(wl)
+    n = 4
+
+    def step(i):
+        toks = (np.arange(n) + i * n) % wl.T
+        oracle.forward_tokens(inp, wl, toks)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    el = time.perf_counter() - t0
+    v = n * args.steps / el
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) x, N(0,0.02) weights, bf16)",
+            "config": {"workload": wl.label, "T": wl.T, "H": wl.H, "F": wl.F, "E": wl.E, "k": wl.k,
+                       "parallelism": "host cores (rank 0 only)"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"each step: {n} tokens of the T={wl.T} batch, float64 numpy oracle"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mixtral", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--T", type=int, default=None)
+    ap.add_argument("--alpha", type=float, default=None)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.workload == "skew" and args.alpha is None:
+        args.alpha = 0.0
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,389 @@
+// Persistent grouped GEMM for the expert FFN on the 5th-generation tensor cores.
+//
+// "Cross-Platform Fused MoE Dispatch in Triton" (review page), "What carries
+// the argument": the gate and up projections of a SwiGLU expert are computed
+// from one shared load of each input tile and SiLU(gate)*up is finished in
+// registers, so the two intermediates never reach global memory; the rest is
+// a grouped GEMM over (expert, token-offset) blocks.  The page's design maps a
+// fixed block size onto a schedule built on the host; here the schedule is
+// built on the device, inside every CTA, from the scanned expert offsets, and
+// the CTAs are persistent, so skewed routing spreads a hot expert's tiles over
+// all SMs instead of stranding them ("Load-bearing premise" / the Zipf skew
+// study name that failure mode).
+//
+// Orientation: weights are the MMA's A operand (M = 128 weight rows of one
+// expert), tokens are B (N = bn tokens, 16..256), so a tile with few tokens
+// still runs a full-height MMA and streams weights at full width.  D^T tiles
+// live in TMEM: lane = output feature, column = token.
+//   SwiGLU:  two accumulators (gate rows, up rows) share every B tile;
+//            epilogue h = SiLU(g) * u -> bf16.
+//   Store:   one accumulator (down projection) -> fp32.
+// Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
+// owner, warps 2-5 epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
+// Pipelines: a ring of `stages` shared-memory slots (full/empty mbarriers) and
+// one or two TMEM accumulator slots (tmem_full/tmem_empty mbarriers).  Every
+// wait is bounded; a wait that gives up records a device error and its role
+// stops.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kMaxStages = 8;
+constexpr int kTileM = 128;
+constexpr int kTileK = 64;
+constexpr int kATileBytes = kTileM * kTileK * 2;  // 16 KB
+constexpr int kMaxSegGroups = 256;
+constexpr int kStagingBytes = 4 * 32 * 32 * 4;    // per-warp 32x32 fp32 transpose tiles
+
+struct SegDev {
+  const int32_t* offsets;
+  int groups, rows, nout, K, bn, ldo;
+  void* out;
+};
+
+struct GemmArgs {
+  SegDev seg[2];
+  int nseg;
+  int stages;
+  int bn_max;
+  int acc_stages;
+  int acc_cols;
+  int tmem_cols;
+  uint32_t* err;
+};
+
+struct Sched {
+  int prefix[2][kMaxSegGroups + 1];    // first tile of each group
+  int rowstart[2][kMaxSegGroups + 1];  // first B row of each group; [G] = end
+  int seg_end[2];                      // tile count after segment 0 / 1
+};
+
+struct Tile {
+  int s, g, mb, tb, a_row, b_row, valid, bn, K;
+};
+
+__device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const Sched& sc, int tile) {
+  Tile t;
+  t.s = (a.nseg > 1 && tile >= sc.seg_end[0]) ? 1 : 0;
+  const SegDev& sg = a.seg[t.s];
+  const int* pre = sc.prefix[t.s];
+  int lo = 0, hi = sg.groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= tile)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  t.g = lo;
+  const int local = tile - pre[lo];
+  const int rows_g = sc.rowstart[t.s][lo + 1] - sc.rowstart[t.s][lo];
+  t.bn = sg.bn;
+  t.K = sg.K;
+  const int ntb = (rows_g + t.bn - 1) / t.bn;
+  t.mb = local / ntb;
+  t.tb = local - t.mb * ntb;
+  t.a_row = lo * sg.nout + t.mb * kTileM;
+  t.b_row = sc.rowstart[t.s][lo] + t.tb * t.bn;
+  t.valid = min(t.bn, rows_g - t.tb * t.bn);
+  return t;
+}
+
+// Tile schedule from the group offsets; run by one warp.
+__device__ void build_schedule(const GemmArgs& a, Sched& sc) {
+  const int lane = threadIdx.x & 31;
+  int total = 0;
+  for (int s = 0; s < a.nseg; ++s) {
+    const SegDev& sg = a.seg[s];
+    const int mblocks = sg.nout / kTileM;
+    for (int base = 0; base < sg.groups; base += 32) {
+      const int g = base + lane;
+      int start = 0, rows_g = 0;
+      if (g < sg.groups) {
+        if (sg.offsets != nullptr) {
+          start = sg.offsets[g];
+          rows_g = sg.offsets[g + 1] - start;
+        } else {
+          rows_g = sg.rows;
+        }
+        // Clamp corrupt offsets so that no tile reaches outside the segment.
+        start = min(max(start, 0), sg.rows);
+        rows_g = min(max(rows_g, 0), sg.rows - start);
+      }
+      const int tiles = (g < sg.groups) ? mblocks * ((rows_g + sg.bn - 1) / sg.bn) : 0;
+      int incl = tiles;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (g < sg.groups) {
+        sc.prefix[s][g] = total + incl - tiles;
+        sc.rowstart[s][g] = start;
+        if (g == sg.groups - 1) sc.rowstart[s][g + 1] = start + rows_g;
+      }
+      total += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (lane == 0) {
+      sc.prefix[s][sg.groups] = total;
+      sc.seg_end[s] = total;
+    }
+  }
+  if (lane == 0 && a.nseg == 1) sc.seg_end[1] = total;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap a0_s0, const __grid_constant__ CUtensorMap a1_s0,
+                        const __grid_constant__ CUtensorMap b_s0, const __grid_constant__ CUtensorMap a0_s1,
+                        const __grid_constant__ CUtensorMap a1_s1, const __grid_constant__ CUtensorMap b_s1,
+                        const GemmArgs a) {
+  constexpr int NUM_A = (EPI == kEpiSwiGLU) ? 2 : 1;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = a.stages;
+  const int stage_bytes = NUM_A * kATileBytes + a.bn_max * kTileK * 2;
+  uint8_t* staging = smem + S * stage_bytes;
+  Sched* sched = reinterpret_cast<Sched*>(staging + kStagingBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sched + 1);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* tfull = empty + kMaxStages;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (warp == 0) build_schedule(a, *sched);
+  if (threadIdx.x == 64) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(tmem_holder, a.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_holder;
+  const Sched& sc = *sched;
+  const int total = sc.seg_end[a.nseg - 1];
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_map(&a0_s0);
+      tma_prefetch_map(&b_s0);
+      if (NUM_A == 2) tma_prefetch_map(&a1_s0);
+      if (a.nseg > 1) {
+        tma_prefetch_map(&a0_s1);
+        tma_prefetch_map(&b_s1);
+        if (NUM_A == 2) tma_prefetch_map(&a1_s1);
+      }
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode_tile(a, sc, tile);
+        const CUtensorMap* ma0 = t.s ? &a0_s1 : &a0_s0;
+        const CUtensorMap* ma1 = t.s ? &a1_s1 : &a1_s0;
+        const CUtensorMap* mb = t.s ? &b_s1 : &b_s0;
+        const uint32_t bytes = NUM_A * kATileBytes + t.bn * kTileK * 2;
+        const int KB = t.K / kTileK;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, a.err, kSiteGemmProducer)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * stage_bytes;
+          mbar_arrive_expect_tx(&full[s], bytes);
+          tma_load_2d(st, ma0, &full[s], kb * kTileK, t.a_row);
+          if (NUM_A == 2) tma_load_2d(st + kATileBytes, ma1, &full[s], kb * kTileK, t.a_row);
+          tma_load_2d(st + NUM_A * kATileBytes, mb, &full[s], kb * kTileK, t.b_row);
+        }
+      }
+      // Do not leave while copies into this CTA's shared memory are in flight.
+      for (int i = (it > S ? it - S : 0); i < it; ++i) mbar_wait(&full[i % S], (i / S) & 1, a.err, kSiteTeardown);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int it = 0, n = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
+        const Tile t = decode_tile(a, sc, tile);
+        const int acc = n % a.acc_stages;
+        const uint32_t aph = (n / a.acc_stages) & 1;
+        if (!mbar_wait(&tempty[acc], aph ^ 1, a.err, kSiteGemmMma)) break;
+        tc_fence_after_sync();
+        const uint32_t d0 = tmem_base + acc * a.acc_cols;
+        const uint32_t d1 = d0 + a.bn_max;
+        const uint32_t idesc = idesc_bf16_f32(kTileM, t.bn);
+        const int KB = t.K / kTileK;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (!mbar_wait(&full[s], ph, a.err, kSiteGemmMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a0 = smem_u32(smem + s * stage_bytes);
+          const uint32_t bb = a0 + NUM_A * kATileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kTileK / 16; ++kk) {
+            const uint64_t bdesc = sdesc_k128(bb + kk * 32);
+            const uint32_t accum = (kb | kk) != 0;
+            umma_bf16(d0, sdesc_k128(a0 + kk * 32), bdesc, idesc, accum);
+            if (NUM_A == 2) umma_bf16(d1, sdesc_k128(a0 + kATileBytes + kk * 32), bdesc, idesc, accum);
+          }
+          umma_commit(&empty[s]);
+        }
+        umma_commit(&tfull[acc]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    uint8_t* stg = staging + (warp - 2) * (32 * 32 * 4);
+    int n = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++n) {
+      const Tile t = decode_tile(a, sc, tile);
+      const int acc = n % a.acc_stages;
+      const uint32_t aph = (n / a.acc_stages) & 1;
+      if (!mbar_wait(&tfull[acc], aph, a.err, kSiteGemmEpilogue)) break;
+      tc_fence_after_sync();
+      const SegDev& sg = a.seg[t.s];
+      const uint32_t col0 = acc * a.acc_cols;
+      const int feat0 = t.mb * kTileM + q * 32;
+      for (int c0 = 0; c0 < t.bn; c0 += 32) {
+        const int nc = min(32, t.bn - c0);
+        uint32_t g[32], u[32];
+        const uint32_t ta = tmem_addr(tmem_base, q * 32, col0 + c0);
+        if (nc == 32) {
+          tmem_ld32(ta, g);
+          if (NUM_A == 2) tmem_ld32(ta + a.bn_max, u);
+        } else {
+          tmem_ld16(ta, g);
+          if (NUM_A == 2) tmem_ld16(ta + a.bn_max, u);
+        }
+        if (NUM_A == 2)
+          tmem_wait(g, u);
+        else
+          tmem_wait(g);
+        if (EPI == kEpiSwiGLU) {
+          __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stg);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j < nc) {
+              const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
+              st[j * 32 + lane] = __float2bfloat16_rn(gv / (1.f + __expf(-gv)) * uv);
+            }
+          }
+          __syncwarp();
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
+          for (int v = lane; v < nc * 4; v += 32) {
+            const int j = v >> 2, piece = v & 3;
+            const int row = t.b_row + c0 + j;
+            if (c0 + j < t.valid && row < sg.rows)
+              *reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * sg.ldo + feat0 + piece * 8) =
+                  *reinterpret_cast<const uint4*>(st + j * 32 + piece * 8);
+          }
+        } else {
+          float* st = reinterpret_cast<float*>(stg);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nc) st[j * 32 + lane] = __uint_as_float(g[j]);
+          __syncwarp();
+          float* out = static_cast<float*>(sg.out);
+          for (int v = lane; v < nc * 8; v += 32) {
+            const int j = v >> 3, piece = v & 7;
+            const int row = t.b_row + c0 + j;
+            if (c0 + j < t.valid && row < sg.rows)
+              *reinterpret_cast<float4*>(out + static_cast<size_t>(row) * sg.ldo + feat0 + piece * 4) =
+                  *reinterpret_cast<const float4*>(st + j * 32 + piece * 4);
+          }
+        }
+        __syncwarp();
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, a.tmem_cols);
+  }
+}
+
+template <int EPI>
+cudaError_t launch_epi(const GemmArgs& a, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* b,
+                       int grid, size_t smem, cudaStream_t stream) {
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         227 * 1024);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const int s1 = a.nseg > 1 ? 1 : 0;
+  grouped_gemm_kernel<EPI><<<grid, kThreads, smem, stream>>>(a0[0], a1[0], b[0], a0[s1], a1[s1], b[s1], a);
+  return cudaGetLastError();
+}
+
+uint32_t pow2_at_least(uint32_t v) {
+  uint32_t p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSegment* segs, const CUtensorMap* a0,
+                                const CUtensorMap* a1, const CUtensorMap* b, int num_sms, uint32_t* err,
+                                cudaStream_t stream) {
+  GemmArgs a{};
+  a.nseg = num_segments;
+  a.err = err;
+  long long upper = 0;
+  for (int s = 0; s < num_segments; ++s) {
+    const GemmSegment& g = segs[s];
+    a.seg[s] = SegDev{g.offsets, g.groups, g.rows, g.nout, g.K, g.bn, g.ldo, g.out};
+    a.bn_max = a.bn_max > g.bn ? a.bn_max : g.bn;
+    upper += static_cast<long long>(g.nout / kTileM) * ((g.rows + g.bn - 1) / g.bn + g.groups);
+  }
+  const int num_a = (epi == kEpiSwiGLU) ? 2 : 1;
+  a.acc_cols = num_a * a.bn_max;
+  a.acc_stages = (2 * a.acc_cols <= 512) ? 2 : 1;
+  a.tmem_cols = static_cast<int>(pow2_at_least(static_cast<uint32_t>(a.acc_stages * a.acc_cols)));
+  const int stage_bytes = num_a * kATileBytes + a.bn_max * kTileK * 2;
+  const int fixed = 1024 + kStagingBytes + static_cast<int>(sizeof(Sched)) + (2 * kMaxStages + 4) * 8 + 64;
+  int stages = (227 * 1024 - fixed) / stage_bytes;
+  if (stages > kMaxStages) stages = kMaxStages;
+  a.stages = stages;
+  const size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(stages) * stage_bytes;
+  int grid = num_sms;
+  if (upper < grid) grid = static_cast<int>(upper);
+  if (grid < 1) grid = 1;
+  if (epi == kEpiSwiGLU) return launch_epi<kEpiSwiGLU>(a, a0, a1, b, grid, smem, stream);
+  return launch_epi<kEpiStoreF32>(a, a0, a1, b, grid, smem, stream);
+}
+
+}  // namespace moe

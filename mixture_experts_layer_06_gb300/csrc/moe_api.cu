@@ -1,0 +1,455 @@
+// C ABI of the MoE layer forward: argument checks, TMA descriptors, workspace
+// carve-up and the launch sequence.  Declarations and contracts: include/moe.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "kernels.h"
+#include "ptx.cuh"
+
+// Device error word (bit 0 timeout, bit 1 bounds, bits 8.. sites).
+__device__ uint32_t g_moe_error_word;
+
+namespace {
+
+using moe::GemmSegment;
+
+constexpr int kMaxDevices = 64;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+  bool ready = false;
+  uint32_t* err = nullptr;
+  int num_sms = 0;
+  void* ws = nullptr;  // moe_forward's cached workspace
+  size_t ws_bytes = 0;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+
+// Stage tracing (moe_set_trace_events).
+constexpr int kTraceEvents = 6;
+cudaEvent_t g_trace[kTraceEvents] = {};
+bool g_trace_on = false;
+
+void trace(int i, cudaStream_t s) {
+  if (g_trace_on) cudaEventRecord(g_trace[i], s);
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Per-device constants, resolved once with that device current.
+moe_status_t device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return MOE_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_moe_error_word) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
+    d.err = static_cast<uint32_t*>(p);
+    d.ready = true;
+  }
+  *out = &d;
+  return MOE_OK;
+}
+
+// bf16 [rows, cols] row-major, box {64 cols, box_rows rows}, 128-byte swizzle,
+// out-of-range rows read as zero.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t check_dims(int T, int H, int F, int E, int k) {
+  if (T < 0 || H <= 0 || F <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_VALUE;
+  if (k > E || E > 256 || k > 16) return MOE_ERR_UNSUPPORTED;
+  if (H % 128 != 0 || F % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(T) * k > (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status_t check_config(const moe_config_t& c, int H, int E, int k) {
+  if (c.score != MOE_SCORE_SOFTMAX && c.score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_VALUE;
+  if (c.n_group > 1) {
+    if (c.n_group > 16 || E % c.n_group != 0) return MOE_ERR_UNSUPPORTED;
+    if (c.topk_group < 1 || c.topk_group > c.n_group) return MOE_ERR_INVALID_VALUE;
+    if (c.group_topn < 1 || c.group_topn > 4 || c.group_topn > E / c.n_group) return MOE_ERR_UNSUPPORTED;
+    if (k > c.topk_group * (E / c.n_group)) return MOE_ERR_INVALID_VALUE;
+  }
+  if (c.logit_bias != nullptr && !aligned16(c.logit_bias)) return MOE_ERR_INVALID_VALUE;
+  if (c.F_shared < 0) return MOE_ERR_INVALID_VALUE;
+  if (c.F_shared > 0) {
+    if (c.F_shared % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!c.ws_gate || !c.ws_up || !c.ws_down) return MOE_ERR_INVALID_VALUE;
+    if (!aligned16(c.ws_gate) || !aligned16(c.ws_up) || !aligned16(c.ws_down)) return MOE_ERR_INVALID_VALUE;
+  }
+  if (c.w_shared_gate != nullptr && !aligned16(c.w_shared_gate)) return MOE_ERR_INVALID_VALUE;
+  (void)H;
+  return MOE_OK;
+}
+
+moe::RouteSpec route_spec(const moe_config_t& c) {
+  moe::RouteSpec s{};
+  s.sigmoid = c.score == MOE_SCORE_SIGMOID;
+  s.renormalize = c.renormalize;
+  s.route_scale = c.route_scale;
+  s.n_group = c.n_group > 1 ? c.n_group : 1;
+  s.topk_group = c.topk_group;
+  s.group_topn = c.group_topn;
+  s.logit_bias = c.logit_bias;
+  return s;
+}
+
+// Token tile of the grouped GEMM: the smallest of 16..256 that covers the
+// mean rows per group.
+int choose_bn(long long rows, int groups) {
+  const long long avg = (rows + groups - 1) / (groups > 0 ? groups : 1);
+  int bn = 16;
+  while (bn < 256 && bn < avg) bn <<= 1;
+  return bn;
+}
+
+// Workspace carve-up of moe_forward_ex, 256-byte aligned pieces.
+struct Layout {
+  size_t topk_idx, topk_w, shared_scale, counts, offsets, perm, inv, scratch, x_perm, h_perm, y_perm, h_shared,
+      y_shared, total;
+};
+
+size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
+
+Layout layout(const moe_config_t& c, int T, int H, int F, int E, int k) {
+  Layout L{};
+  const size_t Tk = static_cast<size_t>(T) * k;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += up256(bytes);
+    return at;
+  };
+  L.topk_idx = take(Tk * 4);
+  L.topk_w = take(Tk * 4);
+  L.shared_scale = take(static_cast<size_t>(T) * 4);
+  L.counts = take(static_cast<size_t>(E) * 4);
+  L.offsets = take(static_cast<size_t>(E + 1) * 4);
+  L.perm = take(Tk * 4);
+  L.inv = take(Tk * 4);
+  L.scratch = take(moe::permute_scratch_bytes(T, E));
+  L.x_perm = take(Tk * H * 2);
+  L.h_perm = take(Tk * F * 2);
+  L.y_perm = take(Tk * H * 4);
+  const size_t Fs = c.F_shared > 0 ? static_cast<size_t>(c.F_shared) : 0;
+  L.h_shared = take(static_cast<size_t>(T) * Fs * 2);
+  L.y_shared = take(Fs ? static_cast<size_t>(T) * H * 4 : 0);
+  L.total = o;
+  return L;
+}
+
+moe_status_t route_impl(DeviceState* d, const moe_config_t& c, const void* x, const void* w_router, int T, int H,
+                        int E, int k, int32_t* topk_idx, float* topk_w, float* shared_scale, cudaStream_t stream) {
+  CUtensorMap mx, mw;
+  const uint32_t ne = static_cast<uint32_t>((E + 15) / 16 * 16);
+  if (!make_map(&mx, x, T, H, 128) || !make_map(&mw, w_router, E, H, ne)) return MOE_ERR_CUDA;
+  cudaError_t e = moe::launch_router(mx, mw, T, H, E, k, route_spec(c), topk_idx, topk_w, d->err, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (c.w_shared_gate != nullptr && shared_scale != nullptr) {
+    e = moe::launch_shared_gate(x, c.w_shared_gate, T, H, shared_scale, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status_t permute_impl(DeviceState* d, const int32_t* topk_idx, const void* x, int T, int H, int E, int k,
+                          int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, void* x_perm,
+                          void* scratch, cudaStream_t stream) {
+  if (T == 0) {
+    if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), stream) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  return cuda_status(
+      moe::launch_permute(topk_idx, x, T, H, E, k, counts, offsets, perm, inv, x_perm, scratch, d->err, stream));
+}
+
+// The two persistent GEMM launches (gate+up, then down) over the routed
+// experts and, when given, the shared expert as a second segment.
+struct FfnOperands {
+  const void* x_rows;  // B of gate+up
+  const int32_t* offsets;
+  int rows, groups, H, F;
+  const void *w_gate, *w_up, *w_down;
+  void* h;
+  float* y;
+};
+
+moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStream_t stream, bool traced = false) {
+  CUtensorMap a0[2], a1[2], b[2];
+  GemmSegment seg[2];
+  for (int s = 0; s < nseg; ++s) {
+    const FfnOperands& o = ops[s];
+    const int bn = choose_bn(o.rows, o.groups);
+    const uint64_t wrows = static_cast<uint64_t>(o.groups) * o.F;
+    if (!make_map(&a0[s], o.w_gate, wrows, o.H, 128) || !make_map(&a1[s], o.w_up, wrows, o.H, 128) ||
+        !make_map(&b[s], o.x_rows, o.rows, o.H, bn))
+      return MOE_ERR_CUDA;
+    seg[s] = GemmSegment{o.offsets, o.groups, o.rows, o.F, o.H, bn, o.h, o.F};
+  }
+  if (moe::launch_grouped_gemm(moe::kEpiSwiGLU, nseg, seg, a0, a1, b, d->num_sms, d->err, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  for (int s = 0; s < nseg; ++s) {
+    const FfnOperands& o = ops[s];
+    const int bn = seg[s].bn;
+    const uint64_t wrows = static_cast<uint64_t>(o.groups) * o.H;
+    if (!make_map(&a0[s], o.w_down, wrows, o.F, 128) || !make_map(&b[s], o.h, o.rows, o.F, bn)) return MOE_ERR_CUDA;
+    a1[s] = a0[s];
+    seg[s] = GemmSegment{o.offsets, o.groups, o.rows, o.H, o.F, bn, o.y, o.H};
+  }
+  if (traced) trace(3, stream);
+  if (moe::launch_grouped_gemm(moe::kEpiStoreF32, nseg, seg, a0, a1, b, d->num_sms, d->err, stream) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void moe_config_default(moe_config_t* cfg) {
+  if (cfg == nullptr) return;
+  std::memset(cfg, 0, sizeof(*cfg));
+  cfg->score = MOE_SCORE_SOFTMAX;
+  cfg->renormalize = 1;
+  cfg->route_scale = 1.0f;
+  cfg->n_group = 1;
+  cfg->topk_group = 1;
+  cfg->group_topn = 0;
+}
+
+int moe_abi_version(void) { return 100; }
+
+moe_status_t moe_set_trace_events(void* const* events, int count) {
+  if (events == nullptr || count == 0) {
+    g_trace_on = false;
+    return MOE_OK;
+  }
+  if (count != kTraceEvents) return MOE_ERR_INVALID_VALUE;
+  for (int i = 0; i < kTraceEvents; ++i) {
+    if (events[i] == nullptr) return MOE_ERR_INVALID_VALUE;
+    g_trace[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  g_trace_on = true;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_VALUE: return "MOE_ERR_INVALID_VALUE";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+    case MOE_ERR_DEVICE_BOUNDS: return "MOE_ERR_DEVICE_BOUNDS";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_router, int T, int H, int E, int k,
+                       int32_t* topk_idx, float* topk_w, float* shared_scale, moe_stream_t stream) {
+  moe_config_t c;
+  if (cfg)
+    c = *cfg;
+  else
+    moe_config_default(&c);
+  moe_status_t st = check_dims(T, H, 128, E, k);
+  if (st != MOE_OK) return st;
+  if ((st = check_config(c, H, E, k)) != MOE_OK) return st;
+  if (!x || !w_router || !topk_idx || !topk_w) return MOE_ERR_INVALID_VALUE;
+  if (c.w_shared_gate && !shared_scale) return MOE_ERR_INVALID_VALUE;
+  if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_VALUE;
+  if (T == 0) return MOE_OK;
+  DeviceState* d = nullptr;
+  if ((st = device_state(&d)) != MOE_OK) return st;
+  return route_impl(d, c, x, w_router, T, H, E, k, topk_idx, topk_w, shared_scale,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t moe_permute_scratch_bytes(int T, int E) {
+  if (T < 0 || E <= 0) return 0;
+  return moe::permute_scratch_bytes(T, E);
+}
+
+moe_status_t moe_permute(const int32_t* topk_idx, const void* x, int T, int H, int E, int k, int32_t* counts,
+                         int32_t* offsets, int32_t* perm, int32_t* inv, void* x_perm, void* scratch,
+                         size_t scratch_bytes, moe_stream_t stream) {
+  moe_status_t st = check_dims(T, H, 128, E, k);
+  if (st != MOE_OK) return st;
+  if (!counts || !offsets) return MOE_ERR_INVALID_VALUE;
+  if (T > 0 && (!topk_idx || !x || !perm || !inv || !x_perm || !scratch)) return MOE_ERR_INVALID_VALUE;
+  if (!aligned16(x) || !aligned16(x_perm) || !aligned16(scratch)) return MOE_ERR_INVALID_VALUE;
+  if (T > 0 && scratch_bytes < moe::permute_scratch_bytes(T, E)) return MOE_ERR_WORKSPACE;
+  DeviceState* d = nullptr;
+  if ((st = device_state(&d)) != MOE_OK) return st;
+  return permute_impl(d, topk_idx, x, T, H, E, k, counts, offsets, perm, inv, x_perm, scratch,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_expert_ffn(const void* x_perm, const int32_t* offsets, int rows, int H, int F, int E,
+                            const void* w_gate, const void* w_up, const void* w_down, void* h, float* y,
+                            moe_stream_t stream) {
+  moe_status_t st = check_dims(rows, H, F, E, 1);
+  if (st != MOE_OK) return st;
+  if (offsets == nullptr && E != 1) return MOE_ERR_INVALID_VALUE;
+  if (rows == 0) return MOE_OK;
+  if (!x_perm || !w_gate || !w_up || !w_down || !h || !y) return MOE_ERR_INVALID_VALUE;
+  if (!aligned16(x_perm) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(h) ||
+      !aligned16(y))
+    return MOE_ERR_INVALID_VALUE;
+  DeviceState* d = nullptr;
+  if ((st = device_state(&d)) != MOE_OK) return st;
+  FfnOperands o{x_perm, offsets, rows, E, H, F, w_gate, w_up, w_down, h, y};
+  return ffn_impl(d, 1, &o, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_combine(const float* y_perm, const int32_t* inv, const float* topk_w, const float* y_shared,
+                         const float* shared_scale, int T, int H, int k, void* out, moe_stream_t stream) {
+  if (T < 0 || H <= 0 || k <= 0 || k > 16) return MOE_ERR_INVALID_VALUE;
+  if (H % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!y_perm || !inv || !topk_w || !out) return MOE_ERR_INVALID_VALUE;
+  if (!aligned16(y_perm) || !aligned16(out) || !aligned16(y_shared)) return MOE_ERR_INVALID_VALUE;
+  return cuda_status(moe::launch_combine(y_perm, inv, topk_w, y_shared, shared_scale, T, H, k, out,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_workspace_bytes(const moe_config_t* cfg, int T, int H, int F, int E, int k) {
+  moe_config_t c;
+  if (cfg)
+    c = *cfg;
+  else
+    moe_config_default(&c);
+  if (check_dims(T, H, F, E, k) != MOE_OK) return 0;
+  return layout(c, T, H, F, E, k).total;
+}
+
+moe_status_t moe_forward_ex(const moe_config_t* cfg, const void* x, const void* w_router, const void* w_gate,
+                            const void* w_up, const void* w_down, int T, int H, int F, int E, int k, void* out,
+                            void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  moe_config_t c;
+  if (cfg)
+    c = *cfg;
+  else
+    moe_config_default(&c);
+  moe_status_t st = check_dims(T, H, F, E, k);
+  if (st != MOE_OK) return st;
+  if ((st = check_config(c, H, E, k)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_router || !w_gate || !w_up || !w_down || !out || !workspace) return MOE_ERR_INVALID_VALUE;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+      !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MOE_ERR_INVALID_VALUE;
+  const Layout L = layout(c, T, H, F, E, k);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+  DeviceState* d = nullptr;
+  if ((st = device_state(&d)) != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto at = [&](size_t off) { return static_cast<void*>(ws + off); };
+  int32_t* topk_idx = static_cast<int32_t*>(at(L.topk_idx));
+  float* topk_w = static_cast<float*>(at(L.topk_w));
+  float* shared_scale = c.w_shared_gate ? static_cast<float*>(at(L.shared_scale)) : nullptr;
+  int32_t* offsets = static_cast<int32_t*>(at(L.offsets));
+  int32_t* inv = static_cast<int32_t*>(at(L.inv));
+  const int Tk = T * k;
+
+  trace(0, s);
+  if ((st = route_impl(d, c, x, w_router, T, H, E, k, topk_idx, topk_w, shared_scale, s)) != MOE_OK) return st;
+  trace(1, s);
+  if ((st = permute_impl(d, topk_idx, x, T, H, E, k, static_cast<int32_t*>(at(L.counts)), offsets,
+                         static_cast<int32_t*>(at(L.perm)), inv, at(L.x_perm), at(L.scratch), s)) != MOE_OK)
+    return st;
+  FfnOperands ops[2];
+  ops[0] = FfnOperands{at(L.x_perm), offsets, Tk, E, H, F, w_gate, w_up, w_down, at(L.h_perm),
+                       static_cast<float*>(at(L.y_perm))};
+  int nseg = 1;
+  float* y_shared = nullptr;
+  if (c.F_shared > 0) {
+    y_shared = static_cast<float*>(at(L.y_shared));
+    ops[1] = FfnOperands{x, nullptr, T, 1, H, c.F_shared, c.ws_gate, c.ws_up, c.ws_down, at(L.h_shared), y_shared};
+    nseg = 2;
+  }
+  trace(2, s);
+  if ((st = ffn_impl(d, nseg, ops, s, true)) != MOE_OK) return st;
+  trace(4, s);
+  st = cuda_status(moe::launch_combine(static_cast<float*>(at(L.y_perm)), inv, topk_w, y_shared, shared_scale, T,
+                                       H, k, out, s));
+  trace(5, s);
+  return st;
+}
+
+moe_status_t moe_forward(const void* x, const void* w_router, const void* w_gate, const void* w_up,
+                         const void* w_down, int T, int H, int F, int E, int k, void* out, moe_stream_t stream) {
+  moe_config_t c;
+  moe_config_default(&c);
+  moe_status_t st = check_dims(T, H, F, E, k);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  DeviceState* d = nullptr;
+  if ((st = device_state(&d)) != MOE_OK) return st;
+  const size_t need = layout(c, T, H, F, E, k).total;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (d->ws_bytes < need) {
+      if (d->ws != nullptr && cudaFreeAsync(d->ws, s) != cudaSuccess) return MOE_ERR_CUDA;
+      d->ws = nullptr;
+      d->ws_bytes = 0;
+      if (cudaMallocAsync(&d->ws, need, s) != cudaSuccess) return MOE_ERR_CUDA;
+      d->ws_bytes = need;
+    }
+    ws = d->ws;
+  }
+  return moe_forward_ex(&c, x, w_router, w_gate, w_up, w_down, T, H, F, E, k, out, ws, need, stream);
+}
+
+moe_status_t moe_device_error(moe_stream_t stream, uint32_t* raw) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t w = 0;
+  if (cudaMemcpyFromSymbol(&w, g_moe_error_word, sizeof(w)) != cudaSuccess) return MOE_ERR_CUDA;
+  const uint32_t zero = 0;
+  if (cudaMemcpyToSymbol(g_moe_error_word, &zero, sizeof(zero)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (raw) *raw = w;
+  if (w & moe::kErrTimeout) return MOE_ERR_DEVICE_TIMEOUT;
+  if (w & moe::kErrBounds) return MOE_ERR_DEVICE_BOUNDS;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,158 @@
+// Token permutation onto experts.
+//
+// "Cross-Platform Fused MoE Dispatch in Triton" (review page), "The reading":
+// after scoring, the tokens are reordered onto experts so that each expert's
+// rows are contiguous for a variable-size GEMM.  The order inside an expert is
+// the token order (a stable counting sort by expert id).
+//
+// Instead of atomics, the sort is built from per-expert token bitmaps:
+//   bitmap[w][e] bit b  <=> token 32*w + b picked expert e
+//   rank of (t, e)      =  offsets[e] + sum_{w' < w} popc(bitmap[w'][e])
+//                          + popc(bitmap[w][e] & lanes below b)
+// which is deterministic and stable by construction.  Three launches:
+//   1. bitmap_kernel: one warp per 32 tokens, __match_any_sync groups lanes by
+//      expert, one word per (word, expert) written, coalesced;
+//   2. scan_kernel: one CTA; per-expert popcount prefix over words, counts,
+//      offsets (exclusive scan), and rowbase[w][e] = first grouped row of word w;
+//   3. gather_kernel: one warp per token computes its k grouped rows, writes
+//      perm / inv and copies x[t] into those rows with 16-byte vectors.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+__global__ void bitmap_kernel(const int32_t* __restrict__ idx, int T, int E, int k, int W,
+                              uint32_t* __restrict__ bitmap, uint32_t* err) {
+  __shared__ uint32_t words[kWarpsPerBlock][256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = blockIdx.x * kWarpsPerBlock + warp;
+  if (w >= W) return;  // warp-uniform
+  uint32_t* mine = words[warp];
+  for (int e = lane; e < E; e += 32) mine[e] = 0;
+  __syncwarp();
+  const int t = w * 32 + lane;
+  for (int j = 0; j < k; ++j) {
+    int e = -1;
+    if (t < T) {
+      e = idx[static_cast<size_t>(t) * k + j];
+      if (e < 0 || e >= E) {
+        raise_error(err, kErrBounds, kSitePermuteIndex);
+        e = -1;
+      }
+    }
+    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) {
+      if (mine[e] & peers) raise_error(err, kErrBounds, kSitePermuteIndex);  // expert repeated in a token
+      mine[e] |= peers;
+    }
+    __syncwarp();
+  }
+  for (int e = lane; e < E; e += 32) bitmap[static_cast<size_t>(w) * E + e] = mine[e];
+}
+
+__global__ void __launch_bounds__(1024, 1)
+    scan_kernel(const uint32_t* __restrict__ bitmap, int W, int E, int32_t* __restrict__ counts,
+                int32_t* __restrict__ offsets, uint32_t* __restrict__ rowbase) {
+  __shared__ uint32_t partial[1024];
+  __shared__ int32_t off_s[257];
+  const int tid = threadIdx.x;
+  const int nc = 1024 / E;  // chunks of words per expert
+  const int e = tid % E, c = tid / E;
+  const bool active = c < nc;
+  const int L = (W + nc - 1) / nc;
+  const int w0 = c * L, w1 = min(W, w0 + L);
+
+  uint32_t sum = 0;
+  if (active)
+    for (int w = w0; w < w1; ++w) sum += __popc(bitmap[static_cast<size_t>(w) * E + e]);
+  partial[tid] = sum;
+  __syncthreads();
+  if (tid < E) {
+    uint32_t run = 0;
+    for (int cc = 0; cc < nc; ++cc) {
+      const uint32_t v = partial[cc * E + tid];
+      partial[cc * E + tid] = run;
+      run += v;
+    }
+    counts[tid] = static_cast<int32_t>(run);
+    off_s[tid] = static_cast<int32_t>(run);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int32_t run = 0;
+    for (int ee = 0; ee < E; ++ee) {
+      const int32_t v = off_s[ee];
+      off_s[ee] = run;
+      run += v;
+    }
+    off_s[E] = run;
+  }
+  __syncthreads();
+  for (int ee = tid; ee <= E; ee += 1024) offsets[ee] = off_s[ee];
+  if (active) {
+    uint32_t run = static_cast<uint32_t>(off_s[e]) + partial[tid];
+    for (int w = w0; w < w1; ++w) {
+      rowbase[static_cast<size_t>(w) * E + e] = run;
+      run += __popc(bitmap[static_cast<size_t>(w) * E + e]);
+    }
+  }
+}
+
+__global__ void gather_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int T, int H8, int E,
+                              int k, const uint32_t* __restrict__ bitmap, const uint32_t* __restrict__ rowbase,
+                              int32_t* __restrict__ perm, int32_t* __restrict__ inv, uint4* __restrict__ x_perm,
+                              uint32_t* err) {
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= T) return;  // warp-uniform
+  const int rows = T * k;
+  int r = -1;
+  if (lane < k) {
+    const int e = idx[static_cast<size_t>(t) * k + lane];
+    if (e >= 0 && e < E) {
+      const size_t we = static_cast<size_t>(t >> 5) * E + e;
+      r = static_cast<int>(rowbase[we] + __popc(bitmap[we] & ((1u << (t & 31)) - 1u)));
+      if (r >= rows) {
+        raise_error(err, kErrBounds, kSitePermuteIndex);
+        r = -1;
+      }
+    }
+    if (r >= 0) perm[r] = t * k + lane;
+    inv[static_cast<size_t>(t) * k + lane] = r;
+  }
+  const uint4* src = x + static_cast<size_t>(t) * H8;
+  for (int v = lane; v < H8; v += 32) {
+    const uint4 val = src[v];
+    for (int j = 0; j < k; ++j) {
+      const int rj = __shfl_sync(0xFFFFFFFFu, r, j);
+      if (rj >= 0) x_perm[static_cast<size_t>(rj) * H8 + v] = val;
+    }
+  }
+}
+
+}  // namespace
+
+size_t permute_scratch_bytes(int T, int E) {
+  const size_t W = (static_cast<size_t>(T) + 31) / 32;
+  return 2 * W * static_cast<size_t>(E) * sizeof(uint32_t) + 256;
+}
+
+cudaError_t launch_permute(const int32_t* topk_idx, const void* x, int T, int H, int E, int k, int32_t* counts,
+                           int32_t* offsets, int32_t* perm, int32_t* inv, void* x_perm, void* scratch,
+                           uint32_t* err, cudaStream_t stream) {
+  const int W = (T + 31) / 32;
+  uint32_t* bitmap = static_cast<uint32_t*>(scratch);
+  uint32_t* rowbase = bitmap + static_cast<size_t>(W) * E;
+  const int threads = kWarpsPerBlock * 32;
+  bitmap_kernel<<<(W + kWarpsPerBlock - 1) / kWarpsPerBlock, threads, 0, stream>>>(topk_idx, T, E, k, W, bitmap,
+                                                                                 err);
+  scan_kernel<<<1, 1024, 0, stream>>>(bitmap, W, E, counts, offsets, rowbase);
+  gather_kernel<<<(T + kWarpsPerBlock - 1) / kWarpsPerBlock, threads, 0, stream>>>(
+      topk_idx, static_cast<const uint4*>(x), T, H / 8, E, k, bitmap, rowbase, perm, inv,
+      static_cast<uint4*>(x_perm), err);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,201 @@
+"""Stage-by-stage parity of the CUDA path with the oracle, through the C ABI.
+
+Each stage is driven by inputs from the seeded generator (not by another
+stage's GPU output), at sizes that span several tiles and ragged tails.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_layer_06_gb300 as moe
+import oracle
+import synth
+from synth.workloads import Workload
+
+from gpu_util import (check_routing, dev_bf16, dev_f32, dev_i32, device_inputs, host_bits, host_f64, make_cfg)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    moe.load_library()
+
+
+# ----------------------------------------------------------------------------- router
+
+ROUTER_CASES = [
+    ("tiny", 128, {}), ("tiny", 1, {}), ("tiny", 200, {}),
+    ("mixtral", 300, {}),
+    ("qwen2", 256, {}),
+    ("skew", 256, {"alpha": 0.0}), ("skew", 512, {"alpha": 1.0}), ("skew", 512, {"alpha": 2.0}),
+    ("deepseek", 512, {}),
+]
+
+
+@pytest.mark.parametrize("name,T,kw", ROUTER_CASES, ids=[f"{c[0]}-T{c[1]}-{c[2]}" for c in ROUTER_CASES])
+def test_route(name, T, kw):
+    wl = synth.workload(name, T=T, **kw)
+    inp = synth.make_inputs(wl, with_experts=False)
+    d = device_inputs(inp)
+    cfg = make_cfg(wl, d)
+    idx, w, ss = moe.moe_route(d["x"], d["w_router"], wl.k, cfg)
+    st, raw = moe.moe_device_error()
+    assert st == 0, raw
+    r = oracle.Routing.of(wl)
+    logits = oracle.router_logits(inp["x"], inp["w_router"], inp.get("logit_bias"))
+    scores = oracle.router_scores(logits, r.score)
+    o_idx = oracle.select_experts(scores, wl.k, r)
+    orc = {"idx": o_idx, "scores": scores, "w": oracle.routing_weights(scores, o_idx, r),
+           "margin": oracle.selection_margin(scores, wl.k, r)}
+    same = check_routing(wl, idx.cpu().numpy(), w.cpu().numpy(), orc)
+    assert same.mean() > 0.95
+    if wl.shared_gate:
+        xf = oracle.widen(inp["x"])
+        want = 1.0 / (1.0 + np.exp(-(xf @ oracle.widen(inp["w_shared_gate"]))))
+        np.testing.assert_allclose(ss.cpu().numpy(), want, rtol=1e-5, atol=1e-6)
+
+
+def test_route_equal_logits_and_one_hot_bias():
+    wl = Workload("t", T=70, H=256, F=128, E=16, k=4)
+    x = synth.normal_bf16(0, 0, (70, 256))
+    wr = np.zeros((16, 256), dtype=np.uint16)
+    idx, w, _ = moe.moe_route(dev_bf16(x), dev_bf16(wr), 4)
+    assert np.all(idx.cpu().numpy() == np.arange(4)[None, :])  # ties -> lowest ids
+    np.testing.assert_allclose(w.cpu().numpy(), 0.25, rtol=1e-6)
+    bias = np.zeros(16, dtype=np.float32)
+    bias[11] = 30.0
+    cfg = moe.MoeConfig.make(logit_bias=dev_f32(bias))
+    idx, w, _ = moe.moe_route(dev_bf16(x), dev_bf16(wr), 1, cfg)
+    assert np.all(idx.cpu().numpy() == 11)
+    np.testing.assert_allclose(w.cpu().numpy(), 1.0)
+
+
+# ----------------------------------------------------------------------------- permute
+
+PERMUTE_CASES = [(1, 8, 2, 0.0, 512), (37, 8, 2, 0.0, 512), (1000, 64, 4, 0.0, 256), (1000, 64, 4, 2.0, 128),
+                 (4096, 8, 2, 1.0, 128), (3000, 256, 8, 0.0, 256), (8192, 256, 8, 1.5, 128), (33, 3, 3, 0.0, 128)]
+
+
+@pytest.mark.parametrize("T,E,k,alpha,H", PERMUTE_CASES)
+def test_permute(T, E, k, alpha, H):
+    idx = synth.random_topk(3, T, E, k, alpha=alpha)
+    x = synth.normal_bf16(3, 50, (T, H))
+    counts, offsets, perm, inv, x_perm = moe.moe_permute(dev_i32(idx), dev_bf16(x), E)
+    st, raw = moe.moe_device_error()
+    assert st == 0, raw
+    c, o, p, i = oracle.permute(idx, E)
+    assert np.array_equal(counts.cpu().numpy(), c)
+    assert np.array_equal(offsets.cpu().numpy(), o)
+    assert np.array_equal(perm.cpu().numpy(), p)
+    assert np.array_equal(inv.cpu().numpy(), i)
+    assert np.array_equal(host_bits(x_perm), x[p // k])
+
+
+def test_permute_rejects_out_of_range_expert_on_device():
+    idx = synth.random_topk(3, 100, 8, 2)
+    idx[17, 1] = 999
+    idx[40, 0] = -3
+    counts, offsets, perm, inv, _ = moe.moe_permute(dev_i32(idx), dev_bf16(synth.normal_bf16(3, 1, (100, 128))), 8)
+    st, raw = moe.moe_device_error()
+    assert st == 6 and raw & 2
+    assert counts.cpu().numpy().sum() == 198
+    iv = inv.cpu().numpy()
+    assert iv[17 * 2 + 1] == -1 and iv[40 * 2] == -1
+    assert moe.moe_device_error()[0] == 0  # cleared
+
+
+# ----------------------------------------------------------------------------- expert FFN
+
+def _ffn_case(rows_per_group, H, F, seed=9):
+    """Grouped rows with the given per-group counts; weights ~ N(0, 0.02)."""
+    E = len(rows_per_group)
+    counts = np.array(rows_per_group, dtype=np.int64)
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    R = int(offsets[-1])
+    xp = synth.normal_bf16(seed, 60, (R, H))
+    wg = synth.normal_bf16(seed, 61, (E, F, H), std=0.02)
+    wu = synth.normal_bf16(seed, 62, (E, F, H), std=0.02)
+    wd = synth.normal_bf16(seed, 63, (E, H, F), std=0.02)
+    return xp, offsets, wg, wu, wd
+
+
+def _oracle_ffn(xp, offsets, wg, wu, wd):
+    xf = oracle.widen(xp)
+    E = wg.shape[0]
+    h = np.zeros((xf.shape[0], wg.shape[1]))
+    y = np.zeros((xf.shape[0], wd.shape[1]))
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        if b > a:
+            g = xf[a:b] @ oracle.widen(wg[e]).T
+            u = xf[a:b] @ oracle.widen(wu[e]).T
+            h[a:b] = g / (1 + np.exp(-g)) * u
+            y[a:b] = oracle.swiglu_expert(xf[a:b], wg[e], wu[e], wd[e])
+    return h, y
+
+
+FFN_CASES = [
+    ("ragged_small", [5, 0, 17, 1, 30, 0, 0, 11], 512, 1024),
+    ("bn16", [3, 9, 14, 16, 7, 1, 12, 2], 256, 384),
+    ("bn32", [31, 20, 33, 25], 384, 256),
+    ("bn64", [64, 70, 1, 55, 60, 66, 0, 80], 512, 512),
+    ("bn128", [128, 100, 129, 150], 256, 640),
+    ("bn256", [300, 257, 200, 255], 512, 512),
+    ("one_expert_all_rows", [0, 0, 333, 0, 0, 0, 0, 0], 512, 1024),
+    ("single_row", [0, 1, 0, 0], 128, 128),
+]
+
+
+@pytest.mark.parametrize("name,counts,H,F", FFN_CASES, ids=[c[0] for c in FFN_CASES])
+def test_expert_ffn(name, counts, H, F):
+    xp, offsets, wg, wu, wd = _ffn_case(counts, H, F)
+    h, y = moe.moe_expert_ffn(dev_bf16(xp), dev_i32(offsets), dev_bf16(wg), dev_bf16(wu), dev_bf16(wd))
+    st, raw = moe.moe_device_error()
+    assert st == 0, raw
+    h_or, y_or = _oracle_ffn(xp, offsets, wg, wu, wd)
+    h_gpu = host_f64(h)
+    # h: one bf16 rounding of an fp32-accumulated value
+    assert np.all(np.abs(h_gpu - h_or) <= 2.0 ** -8 * np.abs(h_or) + 1e-4)
+    y_gpu = host_f64(y)
+    rel = np.linalg.norm(y_gpu - y_or) / np.linalg.norm(y_or)
+    assert rel < 4e-3, rel
+    assert np.abs(y_gpu - y_or).max() <= 1e-2 * np.abs(y_or).max()
+
+
+def test_dense_ffn_matches_plain_swiglu():
+    xp, _, wg, wu, wd = _ffn_case([200], 512, 768)
+    h, y = moe.moe_expert_ffn(dev_bf16(xp), None, dev_bf16(wg[0]), dev_bf16(wu[0]), dev_bf16(wd[0]))
+    assert moe.moe_device_error()[0] == 0
+    y_or = oracle.swiglu_expert(oracle.widen(xp), wg[0], wu[0], wd[0])
+    y_gpu = host_f64(y)
+    assert np.linalg.norm(y_gpu - y_or) / np.linalg.norm(y_or) < 4e-3
+
+
+# ----------------------------------------------------------------------------- combine
+
+@pytest.mark.parametrize("T,k,H,shared", [(1, 2, 128, False), (129, 2, 512, False), (300, 8, 384, True),
+                                          (64, 4, 2048, True)])
+def test_combine(T, k, H, shared):
+    E = 16
+    idx = synth.random_topk(5, T, E, k)
+    _, _, perm, inv = oracle.permute(idx, E)
+    y_perm = synth.normal_f64(5, 70, (T * k, H)).astype(np.float32)
+    w = synth.uniform01(5, 71, T * k).reshape(T, k).astype(np.float32)
+    ys = synth.normal_f64(5, 72, (T, H)).astype(np.float32) if shared else None
+    sc = synth.uniform01(5, 73, T).astype(np.float32) if shared else None
+    out = moe.moe_combine(dev_f32(y_perm), dev_i32(inv), dev_f32(w), dev_f32(ys) if shared else None,
+                          dev_f32(sc) if shared else None)
+    Y = y_perm.astype(np.float64)[inv.reshape(T, k)]
+    want = oracle.combine(Y, w.astype(np.float64))
+    if shared:
+        want = want + sc.astype(np.float64)[:, None] * ys
+    got = host_f64(out)
+    # fp32 sum of k+1 terms rounded once to bf16
+    assert np.all(np.abs(got - want) <= 2.0 ** -8 * np.abs(want) + 1e-5)
+    # deterministic: a second call gives identical bits
+    out2 = moe.moe_combine(dev_f32(y_perm), dev_i32(inv), dev_f32(w), dev_f32(ys) if shared else None,
+                           dev_f32(sc) if shared else None)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
