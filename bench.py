@@ -223,6 +223,9 @@ def run_ours(args):
         ev = None
         if timed_stages:
             ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+            for row in ev:  # create the CUDA events before the timed region
+                for e in row:
+                    e.record(stream)
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             dist.barrier()

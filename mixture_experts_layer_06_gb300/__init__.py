@@ -268,6 +268,9 @@ def moe_set_trace_events(events):
     if events is None:
         _check(lib.moe_set_trace_events(None, 0), "moe_set_trace_events")
         return
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event on first record
+            e.record()
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check(lib.moe_set_trace_events(arr, len(events)), "moe_set_trace_events")
 
