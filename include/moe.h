@@ -201,6 +201,15 @@ MOE_API const char* moe_status_string(moe_status_t status);
 MOE_API moe_status_t moe_device_error(moe_stream_t stream, uint32_t* raw);
 
 /*
+ * Failure-path self-test: launch one block whose single bounded wait has no
+ * producer, so it gives up after limit_us microseconds (1..1000000) and sets
+ * MOE_ERR_DEVICE_TIMEOUT (site bit 17) in the device error word, exactly as a
+ * stalled pipeline wait in the GEMM or router kernels would.  The context
+ * stays usable.  Read the result with moe_device_error().
+ */
+MOE_API moe_status_t moe_selftest_wait_timeout(uint32_t limit_us, moe_stream_t stream);
+
+/*
  * Stage tracing.  When set, every later moe_forward_ex / moe_forward call on
  * any stream records events[i] (cudaEvent_t handles created by the caller)
  * on its stream just before stage i and events[count-1] after the last:

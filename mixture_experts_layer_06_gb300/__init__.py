@@ -18,7 +18,8 @@ import torch
 __all__ = [
     "MoeConfig", "MoeError", "load_library", "library_path", "moe_route", "moe_permute",
     "moe_permute_scratch_bytes", "moe_expert_ffn", "moe_combine", "moe_workspace_bytes", "moe_forward_ex",
-    "moe_forward", "moe_device_error", "moe_set_trace_events", "moe_status_string", "EXPORTED_SYMBOLS",
+    "moe_forward", "moe_device_error", "moe_set_trace_events", "moe_selftest_wait_timeout", "moe_status_string",
+    "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -29,7 +30,7 @@ _lib = None
 EXPORTED_SYMBOLS = (
     "moe_config_default", "moe_route", "moe_permute_scratch_bytes", "moe_permute", "moe_expert_ffn",
     "moe_combine", "moe_workspace_bytes", "moe_forward_ex", "moe_forward", "moe_status_string",
-    "moe_device_error", "moe_set_trace_events", "moe_abi_version",
+    "moe_device_error", "moe_set_trace_events", "moe_selftest_wait_timeout", "moe_abi_version",
 )
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_VALUE", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
@@ -103,6 +104,7 @@ def load_library():
         "moe_status_string": (ctypes.c_char_p, [I]),
         "moe_device_error": (I, [P, ctypes.POINTER(U)]),
         "moe_set_trace_events": (I, [P, I]),
+        "moe_selftest_wait_timeout": (I, [U, P]),
         "moe_abi_version": (I, []),
     }
     for name, (res, args) in sig.items():
@@ -273,6 +275,11 @@ def moe_set_trace_events(events):
             e.record()
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check(lib.moe_set_trace_events(arr, len(events)), "moe_set_trace_events")
+
+
+def moe_selftest_wait_timeout(limit_us: int, stream=None):
+    """Launch the failure-path self-test (a wait nothing releases); see include/moe.h."""
+    _check(load_library().moe_selftest_wait_timeout(limit_us, _stream(stream)), "moe_selftest_wait_timeout")
 
 
 def moe_device_error(stream=None):

@@ -14,6 +14,17 @@
 // Device error word (bit 0 timeout, bit 1 bounds, bits 8.. sites).
 __device__ uint32_t g_moe_error_word;
 
+// One thread waits on an mbarrier that nothing ever arrives on; the bounded
+// wait must give up after limit_ns and record a timeout (failure-path check).
+__global__ void selftest_wait_kernel(uint64_t limit_ns, uint32_t* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    moe::mbar_init(&bar, 1);
+    moe::fence_mbar_init();
+    moe::mbar_wait_for(&bar, 0, limit_ns, err, moe::kSiteSelfTest);
+  }
+}
+
 namespace {
 
 using moe::GemmSegment;
@@ -438,6 +449,15 @@ moe_status_t moe_forward(const void* x, const void* w_router, const void* w_gate
     ws = d->ws;
   }
   return moe_forward_ex(&c, x, w_router, w_gate, w_up, w_down, T, H, F, E, k, out, ws, need, stream);
+}
+
+moe_status_t moe_selftest_wait_timeout(uint32_t limit_us, moe_stream_t stream) {
+  if (limit_us == 0 || limit_us > 1000000u) return MOE_ERR_INVALID_VALUE;
+  DeviceState* d = nullptr;
+  moe_status_t st = device_state(&d);
+  if (st != MOE_OK) return st;
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(uint64_t(limit_us) * 1000u, d->err);
+  return cuda_status(cudaGetLastError());
 }
 
 moe_status_t moe_device_error(moe_stream_t stream, uint32_t* raw) {

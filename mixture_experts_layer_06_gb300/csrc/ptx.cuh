@@ -23,6 +23,7 @@ enum ErrSite : uint32_t {
   kSiteRouterEpilogue = 6,
   kSitePermuteIndex = 7,
   kSiteTeardown = 8,
+  kSiteSelfTest = 9,
 };
 
 __device__ __forceinline__ void raise_error(uint32_t* err, uint32_t kind, uint32_t site) {
@@ -74,17 +75,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity to complete, for at most
-// kWaitLimitNs.  Returns false (and records the site) if it gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t site) {
+// limit_ns.  Returns false (and records the site) if it gave up.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns, uint32_t* err,
+                                              uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       raise_error(err, kErrTimeout, site);
       return false;
     }
   }
   return true;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t site) {
+  return mbar_wait_for(bar, parity, kWaitLimitNs, err, site);
 }
 
 // ------------------------------------------------------------------ TMA

@@ -107,3 +107,8 @@ def test_package_has_no_cpu_fallback():
     import inspect
     src = inspect.getsource(moe)
     assert "oracle" not in src and "numpy" not in src
+
+
+def test_selftest_limit_checked_on_host(lib):
+    assert lib.moe_selftest_wait_timeout(0, None) == 1
+    assert lib.moe_selftest_wait_timeout(2000000, None) == 1

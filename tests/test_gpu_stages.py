@@ -199,3 +199,17 @@ def test_combine(T, k, H, shared):
     out2 = moe.moe_combine(dev_f32(y_perm), dev_i32(inv), dev_f32(w), dev_f32(ys) if shared else None,
                            dev_f32(sc) if shared else None)
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+# ----------------------------------------------------------------------------- failure path
+
+def test_bounded_wait_gives_up_and_context_survives():
+    moe.moe_selftest_wait_timeout(2000)  # a wait nothing releases, 2 ms limit
+    st, raw = moe.moe_device_error()
+    assert st == 5 and (raw & 1) and (raw >> 17) & 1
+    assert moe.moe_device_error()[0] == 0  # the word was cleared
+    # the context is still usable: a full stage runs and is right
+    idx = synth.random_topk(6, 64, 8, 2)
+    x = synth.normal_bf16(6, 1, (64, 128))
+    counts, offsets, perm, inv, x_perm = moe.moe_permute(dev_i32(idx), dev_bf16(x), 8)
+    assert np.array_equal(perm.cpu().numpy(), oracle.permute(idx, 8)[2])
