@@ -294,12 +294,13 @@ def run_ours(args):
     sweep = []
     for T in sweep_T:
         K = max(args.steps, 20) if T <= 32 else args.steps
-        r = run_T(T, K, args.warmup, False)
+        r = run_T(T, K, args.warmup, True)
         w = r["wl"]
         ms = r["ms_total"] / K
         tr = max(w.flops() / NOMINAL_BF16, w.compulsory_bytes(r["active_experts"]) / NOMINAL_HBM)
         sweep.append({"T": T, "tokens_per_s": T / (ms / 1e3), "us_per_step": ms * 1e3,
-                      "layer_roofline_frac": tr / (ms / 1e3), "active_experts": r["active_experts"]})
+                      "layer_roofline_frac": tr / (ms / 1e3), "active_experts": r["active_experts"],
+                      "stages_us": {k2: v * 1e3 for k2, v in r["stage_ms"].items()}})
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,

@@ -138,12 +138,18 @@ moe::RouteSpec route_spec(const moe_config_t& c) {
   return s;
 }
 
-// Token tile of the grouped GEMM: the smallest of 16..256 that covers the
+// Largest token tile of the SwiGLU GEMM.  Its two accumulators take 2*bn
+// TMEM columns, so bn <= 128 leaves room for two accumulator stages.
+#ifndef MOE_SWIGLU_BN_MAX
+#define MOE_SWIGLU_BN_MAX 256
+#endif
+
+// Token tile of the grouped GEMM: the smallest of 16..bn_max that covers the
 // mean rows per group.
-int choose_bn(long long rows, int groups) {
+int choose_bn(long long rows, int groups, int bn_max = 256) {
   const long long avg = (rows + groups - 1) / (groups > 0 ? groups : 1);
   int bn = 16;
-  while (bn < 256 && bn < avg) bn <<= 1;
+  while (bn < bn_max && bn < avg) bn <<= 1;
   return bn;
 }
 
@@ -224,7 +230,7 @@ moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStre
   GemmSegment seg[2];
   for (int s = 0; s < nseg; ++s) {
     const FfnOperands& o = ops[s];
-    const int bn = choose_bn(o.rows, o.groups);
+    const int bn = choose_bn(o.rows, o.groups, MOE_SWIGLU_BN_MAX);
     const uint64_t wrows = static_cast<uint64_t>(o.groups) * o.F;
     if (!make_map(&a0[s], o.w_gate, wrows, o.H, 128) || !make_map(&a1[s], o.w_up, wrows, o.H, 128) ||
         !make_map(&b[s], o.x_rows, o.rows, o.H, bn))
@@ -235,7 +241,7 @@ moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStre
     return MOE_ERR_CUDA;
   for (int s = 0; s < nseg; ++s) {
     const FfnOperands& o = ops[s];
-    const int bn = seg[s].bn;
+    const int bn = choose_bn(o.rows, o.groups);
     const uint64_t wrows = static_cast<uint64_t>(o.groups) * o.H;
     if (!make_map(&a0[s], o.w_down, wrows, o.F, 128) || !make_map(&b[s], o.h, o.rows, o.F, bn)) return MOE_ERR_CUDA;
     a1[s] = a0[s];
