@@ -133,6 +133,29 @@ MOE_API moe_status_t moe_permute(const int32_t* topk_idx, const void* x, int T, 
                          moe_stream_t stream);
 
 /*
+ * moe_permute without caller scratch.  The paper has no counterpart: this
+ * entry point exists for callers that cannot allocate device memory, such as
+ * serving engines that plan all device memory at start-up and forbid any
+ * allocation afterwards, plugins that run inside a host application which
+ * owns the CUDA allocator, and code with latency bounds that cannot afford
+ * cudaMalloc's implicit synchronisation.
+ * Same arguments and results as moe_permute, minus scratch: the token bitmaps
+ * live in a 512 KiB array built into the library's device image (every GPU
+ * that loads the library holds it until the process exits).  Limits: all of
+ * moe_permute's, plus ceil(T/32) * E <= 65536 (e.g. T <= 8192 at E = 256);
+ * larger calls return MOE_ERR_WORKSPACE and launch nothing.  The first call
+ * on each device looks up that device's copy of the array, so make it before
+ * any stream capture.  Every call on a device shares the one array: calls
+ * that overlap on the GPU (different streams, or concurrent host threads)
+ * race and must be serialised by the caller.  Nothing in the array needs to
+ * start at zero; each call writes every word it reads.  Allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library call).
+ */
+MOE_API moe_status_t moe_permute_noalloc(const int32_t* topk_idx, const void* x, int T, int H, int E, int k,
+                                         int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                                         void* x_perm, moe_stream_t stream);
+
+/*
  * Expert SwiGLU FFN over grouped rows ("What carries the argument": a fused
  * gate+up GEMM that finishes SiLU(gate)*up in registers, then a grouped
  * down-projection GEMM; one persistent kernel each, with a tile schedule

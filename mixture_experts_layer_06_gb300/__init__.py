@@ -17,7 +17,7 @@ import torch
 
 __all__ = [
     "MoeConfig", "MoeError", "load_library", "library_path", "moe_route", "moe_permute",
-    "moe_permute_scratch_bytes", "moe_expert_ffn", "moe_combine", "moe_workspace_bytes", "moe_forward_ex",
+    "moe_permute_scratch_bytes", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_workspace_bytes", "moe_forward_ex",
     "moe_forward", "moe_device_error", "moe_set_trace_events", "moe_selftest_wait_timeout", "moe_status_string",
     "EXPORTED_SYMBOLS",
 ]
@@ -31,6 +31,7 @@ EXPORTED_SYMBOLS = (
     "moe_config_default", "moe_route", "moe_permute_scratch_bytes", "moe_permute", "moe_expert_ffn",
     "moe_combine", "moe_workspace_bytes", "moe_forward_ex", "moe_forward", "moe_status_string",
     "moe_device_error", "moe_set_trace_events", "moe_selftest_wait_timeout", "moe_abi_version",
+    "moe_permute_noalloc",
 )
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_VALUE", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
@@ -96,6 +97,7 @@ def load_library():
         "moe_route": (I, [P, P, P, I, I, I, I, P, P, P, P]),
         "moe_permute_scratch_bytes": (S, [I, I]),
         "moe_permute": (I, [P, P, I, I, I, I, P, P, P, P, P, P, S, P]),
+        "moe_permute_noalloc": (I, [P, P, I, I, I, I, P, P, P, P, P, P]),
         "moe_expert_ffn": (I, [P, P, I, I, I, I, P, P, P, P, P, P]),
         "moe_combine": (I, [P, P, P, P, P, I, I, I, P, P]),
         "moe_workspace_bytes": (S, [P, I, I, I, I, I]),
@@ -198,6 +200,27 @@ def moe_permute(topk_idx, x, E, counts=None, offsets=None, perm=None, inv=None, 
                          _ptr(offsets, torch.int32), _ptr(perm, torch.int32), _ptr(inv, torch.int32),
                          _ptr(x_perm), _ptr(scratch, torch.uint8), scratch.numel(), _stream(stream))
     _check(st, "moe_permute")
+    return counts, offsets, perm, inv, x_perm
+
+
+def moe_permute_noalloc(topk_idx, x, E, counts=None, offsets=None, perm=None, inv=None, x_perm=None,
+                        stream=None):
+    """moe_permute with the library's built-in scratch, for callers that cannot allocate device
+    memory (pass every output tensor to allocate nothing here either).
+    Returns (counts, offsets, perm, inv, x_perm)."""
+    lib = load_library()
+    T, k = topk_idx.shape
+    H = x.shape[1]
+    dev = x.device
+    counts = _out(counts, (E,), torch.int32, dev)
+    offsets = _out(offsets, (E + 1,), torch.int32, dev)
+    perm = _out(perm, (T * k,), torch.int32, dev)
+    inv = _out(inv, (T * k,), torch.int32, dev)
+    x_perm = _out(x_perm, (T * k, H), torch.bfloat16, dev)
+    st = lib.moe_permute_noalloc(_ptr(topk_idx, torch.int32), _ptr(x), T, H, E, k, _ptr(counts, torch.int32),
+                                 _ptr(offsets, torch.int32), _ptr(perm, torch.int32), _ptr(inv, torch.int32),
+                                 _ptr(x_perm), _stream(stream))
+    _check(st, "moe_permute_noalloc")
     return counts, offsets, perm, inv, x_perm
 
 

@@ -58,6 +58,10 @@ cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSe
                                 const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* b,
                                 int num_sms, uint32_t* err, cudaStream_t stream);
 
+// Address of the current device's error word (nullptr if the device could
+// not be set up).
+uint32_t* device_error_word();
+
 // Deterministic weighted combine.
 cudaError_t launch_combine(const float* y_perm, const int32_t* inv, const float* topk_w, const float* y_shared,
                            const float* shared_scale, int T, int H, int k, void* out, cudaStream_t stream);

@@ -256,6 +256,13 @@ moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStre
 
 }  // namespace
 
+namespace moe {
+uint32_t* device_error_word() {
+  DeviceState* d = nullptr;
+  return device_state(&d) == MOE_OK ? d->err : nullptr;
+}
+}  // namespace moe
+
 extern "C" {
 
 void moe_config_default(moe_config_t* cfg) {

@@ -16,6 +16,9 @@
 //      offsets (exclusive scan), and rowbase[w][e] = first grouped row of word w;
 //   3. gather_kernel: one warp per token computes its k grouped rows, writes
 //      perm / inv and copies x[t] into those rows with 16-byte vectors.
+#include <mutex>
+
+#include "../../include/moe.h"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -156,3 +159,69 @@ cudaError_t launch_permute(const int32_t* topk_idx, const void* x, int T, int H,
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// moe_permute_noalloc: the same three kernels with their scratch (the token
+// bitmaps and row bases) in a fixed array that lives in this library's device
+// image, so the caller passes no scratch and nothing is allocated.
+
+namespace {
+
+// Words per scratch array; the permute needs ceil(T/32) * E words for each of
+// its two arrays, so calls with ceil(T/32) * E <= kNoAllocWords fit
+// (for example T <= 8192 with E = 256, or T <= 262144 with E = 8).
+constexpr size_t kNoAllocWords = 65536;
+
+// 2 x 256 KiB, held by every GPU that loads the library until the process exits.
+static __device__ __align__(256) uint32_t g_noalloc_scratch[2 * kNoAllocWords];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device, with that device current, and cached.
+moe_status_t noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" MOE_API moe_status_t moe_permute_noalloc(const int32_t* topk_idx, const void* x, int T, int H, int E,
+                                                    int k, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                                    int32_t* inv, void* x_perm, moe_stream_t stream) {
+  if (T < 0 || H <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_VALUE;
+  if (k > E || E > 256 || k > 16 || H % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(T) * k > (1LL << 30)) return MOE_ERR_UNSUPPORTED;
+  const size_t words = (static_cast<size_t>(T) + 31) / 32 * static_cast<size_t>(E);
+  if (words > kNoAllocWords) return MOE_ERR_WORKSPACE;  // beyond the built-in scratch
+  if (!counts || !offsets) return MOE_ERR_INVALID_VALUE;
+  if (T > 0 && (!topk_idx || !x || !perm || !inv || !x_perm)) return MOE_ERR_INVALID_VALUE;
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(x_perm) & 15u))
+    return MOE_ERR_INVALID_VALUE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  void* scratch = nullptr;
+  moe_status_t st = noalloc_scratch(&scratch);
+  if (st != MOE_OK) return st;
+  if (T == 0) {
+    if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  // Every scratch word the kernels read is written earlier in the same call
+  // (bitmap_kernel writes all ceil(T/32) * E bitmap words, scan_kernel all
+  // row bases), so nothing needs clearing between calls.
+  const cudaError_t e = moe::launch_permute(topk_idx, x, T, H, E, k, counts, offsets, perm, inv, x_perm, scratch,
+                                            moe::device_error_word(), s);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
