@@ -98,19 +98,24 @@ MOE_API void moe_config_default(moe_config_t* cfg);
 /*
  * Router scoring and top-k selection ("The reading": tokens are scored).
  * logits = x . W_r^T (+ logit_bias) with fp32 accumulation on the tensor
- * cores, then the score function, top-k and weights as in moe_config_t.
+ * cores (the K dimension split over CTAs, partial logits added in a fixed
+ * order), then the score function, top-k and weights as in moe_config_t.
  *   x:            bf16 [T, H]
  *   w_router:     bf16 [E, H]
  *   topk_idx:     int32 [T, k] out, slot order = descending score
  *   topk_w:       fp32 [T, k] out, routing weights in the same order
  *   shared_scale: fp32 [T] out, sigmoid(x . w_shared_gate); may be NULL
  *                 when cfg->w_shared_gate is NULL.
+ *   scratch:      device memory of at least moe_route_scratch_bytes(cfg, T,
+ *                 H, E) bytes (fp32 partial logits); too little returns
+ *                 MOE_ERR_WORKSPACE.
  * cfg may be NULL (moe_config_default).
  */
+MOE_API size_t moe_route_scratch_bytes(const moe_config_t* cfg, int T, int H, int E);
 MOE_API moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_router,
                        int T, int H, int E, int k,
                        int32_t* topk_idx, float* topk_w, float* shared_scale,
-                       moe_stream_t stream);
+                       void* scratch, size_t scratch_bytes, moe_stream_t stream);
 
 /*
  * Token permutation ("The reading": tokens are reordered onto experts).

@@ -16,7 +16,7 @@ import os
 import torch
 
 __all__ = [
-    "MoeConfig", "MoeError", "load_library", "library_path", "moe_route", "moe_permute",
+    "MoeConfig", "MoeError", "load_library", "library_path", "moe_route", "moe_route_scratch_bytes", "moe_permute",
     "moe_permute_scratch_bytes", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_workspace_bytes", "moe_forward_ex",
     "moe_forward", "moe_device_error", "moe_set_trace_events", "moe_selftest_wait_timeout", "moe_status_string",
     "EXPORTED_SYMBOLS",
@@ -28,7 +28,7 @@ _lib = None
 
 # Entry points declared in include/moe.h.
 EXPORTED_SYMBOLS = (
-    "moe_config_default", "moe_route", "moe_permute_scratch_bytes", "moe_permute", "moe_expert_ffn",
+    "moe_config_default", "moe_route", "moe_route_scratch_bytes", "moe_permute_scratch_bytes", "moe_permute", "moe_expert_ffn",
     "moe_combine", "moe_workspace_bytes", "moe_forward_ex", "moe_forward", "moe_status_string",
     "moe_device_error", "moe_set_trace_events", "moe_selftest_wait_timeout", "moe_abi_version",
     "moe_permute_noalloc",
@@ -94,7 +94,8 @@ def load_library():
     P, I, S, U = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint32
     sig = {
         "moe_config_default": (None, [P]),
-        "moe_route": (I, [P, P, P, I, I, I, I, P, P, P, P]),
+        "moe_route": (I, [P, P, P, I, I, I, I, P, P, P, P, S, P]),
+        "moe_route_scratch_bytes": (S, [P, I, I, I]),
         "moe_permute_scratch_bytes": (S, [I, I]),
         "moe_permute": (I, [P, P, I, I, I, I, P, P, P, P, P, P, S, P]),
         "moe_permute_noalloc": (I, [P, P, I, I, I, I, P, P, P, P, P, P]),
@@ -160,8 +161,12 @@ def moe_status_string(status: int) -> str:
 
 # ----------------------------------------------------------------------------- entry points
 
+def moe_route_scratch_bytes(cfg: MoeConfig | None, T: int, H: int, E: int) -> int:
+    return int(load_library().moe_route_scratch_bytes(ctypes.byref(cfg) if cfg is not None else None, T, H, E))
+
+
 def moe_route(x, w_router, k, cfg: MoeConfig | None = None, topk_idx=None, topk_w=None, shared_scale=None,
-              stream=None):
+              scratch=None, stream=None):
     """Router scoring + top-k.  Returns (topk_idx int32 [T,k], topk_w fp32 [T,k], shared_scale or None)."""
     lib = load_library()
     T, H = x.shape
@@ -170,9 +175,12 @@ def moe_route(x, w_router, k, cfg: MoeConfig | None = None, topk_idx=None, topk_
     topk_w = _out(topk_w, (T, k), torch.float32, x.device)
     if cfg is not None and cfg.w_shared_gate:
         shared_scale = _out(shared_scale, (T,), torch.float32, x.device)
+    if scratch is None:
+        scratch = torch.empty(max(moe_route_scratch_bytes(cfg, T, H, E), 16), dtype=torch.uint8, device=x.device)
     st = lib.moe_route(ctypes.byref(cfg) if cfg is not None else None, _ptr(x), _ptr(w_router), T, H, E, k,
                        _ptr(topk_idx, torch.int32), _ptr(topk_w, torch.float32),
-                       _ptr(shared_scale, torch.float32), _stream(stream))
+                       _ptr(shared_scale, torch.float32), _ptr(scratch, torch.uint8), scratch.numel(),
+                       _stream(stream))
     _check(st, "moe_route")
     return topk_idx, topk_w, shared_scale
 

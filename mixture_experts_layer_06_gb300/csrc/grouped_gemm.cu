@@ -30,6 +30,12 @@
 namespace moe {
 namespace {
 
+// Exact MMA width (compile-time): a token tile with fewer than bn rows runs
+// its MMAs with N = its rows rounded up to 16 (else N = bn).
+#ifndef MOE_EXACT_N
+#define MOE_EXACT_N 1
+#endif
+
 constexpr int kThreads = 192;
 constexpr int kMaxStages = 8;
 constexpr int kTileM = 128;
@@ -40,7 +46,8 @@ constexpr int kStagingBytes = 4 * 32 * 32 * 4;    // per-warp 32x32 fp32 transpo
 
 struct SegDev {
   const int32_t* offsets;
-  int groups, rows, nout, K, bn, ldo;
+  int groups, rows, nout, K, bn, ldo, ksplit;
+  size_t slice_stride;
   void* out;
 };
 
@@ -48,6 +55,7 @@ struct GemmArgs {
   SegDev seg[2];
   int nseg;
   int stages;
+  int kps;  // 64-wide K blocks per pipeline stage (one 3-D TMA box each)
   int bn_max;
   int acc_stages;
   int acc_cols;
@@ -58,11 +66,17 @@ struct GemmArgs {
 struct Sched {
   int prefix[2][kMaxSegGroups + 1];    // first tile of each group
   int rowstart[2][kMaxSegGroups + 1];  // first B row of each group; [G] = end
+  int trows[2][kMaxSegGroups];         // token rows per tile of each group
   int seg_end[2];                      // tile count after segment 0 / 1
 };
 
+struct GemmMaps {
+  SegMaps seg[2];
+};
+
 struct Tile {
-  int s, g, mb, tb, a_row, b_row, valid, bn, K;
+  int s, g, mb, tb, a_row, b_row, valid, bn, kb0, kb1;
+  size_t out_off;  // element offset of this tile's output slice
 };
 
 __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const Sched& sc, int tile) {
@@ -79,16 +93,22 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const Sched& sc, 
       hi = mid - 1;
   }
   t.g = lo;
-  const int local = tile - pre[lo];
+  int local = tile - pre[lo];
   const int rows_g = sc.rowstart[t.s][lo + 1] - sc.rowstart[t.s][lo];
   t.bn = sg.bn;
-  t.K = sg.K;
+  const int ks = local % sg.ksplit;  // K slice, fastest
+  local /= sg.ksplit;
   const int ntb = (rows_g + t.bn - 1) / t.bn;
+  const int tr = sc.trows[t.s][lo];
   t.mb = local / ntb;
   t.tb = local - t.mb * ntb;
   t.a_row = lo * sg.nout + t.mb * kTileM;
-  t.b_row = sc.rowstart[t.s][lo] + t.tb * t.bn;
-  t.valid = min(t.bn, rows_g - t.tb * t.bn);
+  t.b_row = sc.rowstart[t.s][lo] + t.tb * tr;
+  t.valid = min(tr, rows_g - t.tb * tr);
+  const int KB = sg.K / (kTileK * a.kps);  // stages of kps K blocks
+  t.kb0 = ks * KB / sg.ksplit;
+  t.kb1 = (ks + 1) * KB / sg.ksplit;
+  t.out_off = static_cast<size_t>(ks) * sg.slice_stride;
   return t;
 }
 
@@ -113,7 +133,12 @@ __device__ void build_schedule(const GemmArgs& a, Sched& sc) {
         start = min(max(start, 0), sg.rows);
         rows_g = min(max(rows_g, 0), sg.rows - start);
       }
-      const int tiles = (g < sg.groups) ? mblocks * ((rows_g + sg.bn - 1) / sg.bn) : 0;
+      // The token tiles of a group are balanced (equal rows, rounded up to
+      // 16), so that the tiles sharing a weight block stream it through L2
+      // in step instead of a short last tile racing ahead.
+      const int ntb = (rows_g + sg.bn - 1) / sg.bn;
+      const int tiles = (g < sg.groups) ? mblocks * ntb * sg.ksplit : 0;
+      if (g < sg.groups) sc.trows[s][g] = ntb > 0 ? ((rows_g + ntb - 1) / ntb + 15) / 16 * 16 : sg.bn;
       int incl = tiles;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -137,15 +162,13 @@ __device__ void build_schedule(const GemmArgs& a, Sched& sc) {
 
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap a0_s0, const __grid_constant__ CUtensorMap a1_s0,
-                        const __grid_constant__ CUtensorMap b_s0, const __grid_constant__ CUtensorMap a0_s1,
-                        const __grid_constant__ CUtensorMap a1_s1, const __grid_constant__ CUtensorMap b_s1,
-                        const GemmArgs a) {
+    grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
   constexpr int NUM_A = (EPI == kEpiSwiGLU) ? 2 : 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages;
-  const int stage_bytes = NUM_A * kATileBytes + a.bn_max * kTileK * 2;
+  const int KPS = a.kps;
+  const int stage_bytes = KPS * (NUM_A * kATileBytes + a.bn_max * kTileK * 2);
   uint8_t* staging = smem + S * stage_bytes;
   Sched* sched = reinterpret_cast<Sched*>(staging + kStagingBytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(sched + 1);
@@ -182,41 +205,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
+    // One elected lane: wait for a free slot, post the byte count, issue the
+    // loads of the weight tile(s) and of the token tile.  The token box is
+    // always bn rows (one request); rows past the tile's own are not used.
+    // Several smaller boxes per tile were measured to be much slower.
+    int it = 0;
     if (lane == 0) {
-      tma_prefetch_map(&a0_s0);
-      tma_prefetch_map(&b_s0);
-      if (NUM_A == 2) tma_prefetch_map(&a1_s0);
-      if (a.nseg > 1) {
-        tma_prefetch_map(&a0_s1);
-        tma_prefetch_map(&b_s1);
-        if (NUM_A == 2) tma_prefetch_map(&a1_s1);
+      for (int sg = 0; sg < a.nseg; ++sg) {
+        tma_prefetch_map(&maps.seg[sg].a0);
+        if (NUM_A == 2) tma_prefetch_map(&maps.seg[sg].a1);
+        tma_prefetch_map(&maps.seg[sg].b);
       }
-      int it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const Tile t = decode_tile(a, sc, tile);
-        const CUtensorMap* ma0 = t.s ? &a0_s1 : &a0_s0;
-        const CUtensorMap* ma1 = t.s ? &a1_s1 : &a1_s0;
-        const CUtensorMap* mb = t.s ? &b_s1 : &b_s0;
-        const uint32_t bytes = NUM_A * kATileBytes + t.bn * kTileK * 2;
-        const int KB = t.K / kTileK;
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        const SegMaps& m = maps.seg[t.s];
+        const uint32_t bytes = KPS * (NUM_A * kATileBytes + t.bn * kTileK * 2);
+        for (int kb = t.kb0; kb < t.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, a.err, kSiteGemmProducer)) {
             ok = false;
             break;
           }
-          uint8_t* st = smem + s * stage_bytes;
           mbar_arrive_expect_tx(&full[s], bytes);
-          tma_load_2d(st, ma0, &full[s], kb * kTileK, t.a_row);
-          if (NUM_A == 2) tma_load_2d(st + kATileBytes, ma1, &full[s], kb * kTileK, t.a_row);
-          tma_load_2d(st + NUM_A * kATileBytes, mb, &full[s], kb * kTileK, t.b_row);
+          uint8_t* st = smem + s * stage_bytes;
+          uint8_t* sb = st + KPS * NUM_A * kATileBytes;
+          if (KPS == 1) {  // 2-D maps
+            tma_load_2d(st, &m.a0, &full[s], kb * kTileK, t.a_row);
+            if (NUM_A == 2) tma_load_2d(st + kATileBytes, &m.a1, &full[s], kb * kTileK, t.a_row);
+            tma_load_2d(sb, &m.b, &full[s], kb * kTileK, t.b_row);
+          } else {  // 3-D maps: KPS consecutive K blocks per request
+            tma_load_3d(st, &m.a0, &full[s], 0, t.a_row, kb * KPS);
+            if (NUM_A == 2) tma_load_3d(st + KPS * kATileBytes, &m.a1, &full[s], 0, t.a_row, kb * KPS);
+            tma_load_3d(sb, &m.b, &full[s], 0, t.b_row, kb * KPS);
+          }
         }
       }
-      // Do not leave while copies into this CTA's shared memory are in flight.
-      for (int i = (it > S ? it - S : 0); i < it; ++i) mbar_wait(&full[i % S], (i / S) & 1, a.err, kSiteTeardown);
     }
+    // Do not leave while copies into this CTA's shared memory are in flight.
+    if (lane == 0)
+      for (int i = (it > S ? it - S : 0); i < it; ++i) mbar_wait(&full[i % S], (i / S) & 1, a.err, kSiteTeardown);
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -230,9 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t d0 = tmem_base + acc * a.acc_cols;
         const uint32_t d1 = d0 + a.bn_max;
-        const uint32_t idesc = idesc_bf16_f32(kTileM, t.bn);
-        const int KB = t.K / kTileK;
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        const uint32_t idesc = idesc_bf16_f32(kTileM, MOE_EXACT_N ? ((t.valid + 15) >> 4) << 4 : t.bn);
+        for (int kb = t.kb0; kb < t.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
           if (!mbar_wait(&full[s], ph, a.err, kSiteGemmMma)) {
@@ -241,13 +270,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after_sync();
           const uint32_t a0 = smem_u32(smem + s * stage_bytes);
-          const uint32_t bb = a0 + NUM_A * kATileBytes;
+          const uint32_t bb = a0 + KPS * NUM_A * kATileBytes;
+          const uint32_t b_atom = t.bn * kTileK * 2;
+          for (int j = 0; j < KPS; ++j) {
 #pragma unroll
-          for (int kk = 0; kk < kTileK / 16; ++kk) {
-            const uint64_t bdesc = sdesc_k128(bb + kk * 32);
-            const uint32_t accum = (kb | kk) != 0;
-            umma_bf16(d0, sdesc_k128(a0 + kk * 32), bdesc, idesc, accum);
-            if (NUM_A == 2) umma_bf16(d1, sdesc_k128(a0 + kATileBytes + kk * 32), bdesc, idesc, accum);
+            for (int kk = 0; kk < kTileK / 16; ++kk) {
+              const uint64_t bdesc = sdesc_k128(bb + j * b_atom + kk * 32);
+              const uint32_t accum = (kb != t.kb0 || j != 0 || kk != 0);
+              umma_bf16(d0, sdesc_k128(a0 + j * kATileBytes + kk * 32), bdesc, idesc, accum);
+              if (NUM_A == 2)
+                umma_bf16(d1, sdesc_k128(a0 + (KPS + j) * kATileBytes + kk * 32), bdesc, idesc, accum);
+            }
           }
           umma_commit(&empty[s]);
         }
@@ -268,8 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const SegDev& sg = a.seg[t.s];
       const uint32_t col0 = acc * a.acc_cols;
       const int feat0 = t.mb * kTileM + q * 32;
-      for (int c0 = 0; c0 < t.bn; c0 += 32) {
-        const int nc = min(32, t.bn - c0);
+      const int ncols = MOE_EXACT_N ? ((t.valid + 15) >> 4) << 4 : t.bn;  // the columns the MMA wrote
+      for (int c0 = 0; c0 < ncols; c0 += 32) {
+        const int nc = min(32, ncols - c0);
         uint32_t g[32], u[32];
         const uint32_t ta = tmem_addr(tmem_base, q * 32, col0 + c0);
         if (nc == 32) {
@@ -307,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 32; ++j)
             if (j < nc) st[j * 32 + lane] = __uint_as_float(g[j]);
           __syncwarp();
-          float* out = static_cast<float*>(sg.out);
+          float* out = static_cast<float*>(sg.out) + t.out_off;
           for (int v = lane; v < nc * 8; v += 32) {
             const int j = v >> 3, piece = v & 7;
             const int row = t.b_row + c0 + j;
@@ -332,8 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int EPI>
-cudaError_t launch_epi(const GemmArgs& a, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* b,
-                       int grid, size_t smem, cudaStream_t stream) {
+cudaError_t launch_epi(const GemmArgs& a, const GemmMaps& maps, int grid, size_t smem, cudaStream_t stream) {
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -343,8 +376,7 @@ cudaError_t launch_epi(const GemmArgs& a, const CUtensorMap* a0, const CUtensorM
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int s1 = a.nseg > 1 ? 1 : 0;
-  grouped_gemm_kernel<EPI><<<grid, kThreads, smem, stream>>>(a0[0], a1[0], b[0], a0[s1], a1[s1], b[s1], a);
+  grouped_gemm_kernel<EPI><<<grid, kThreads, smem, stream>>>(maps, a);
   return cudaGetLastError();
 }
 
@@ -354,27 +386,58 @@ uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
+constexpr int kFixedSmem = 1024 + kStagingBytes + static_cast<int>(sizeof(Sched)) + (2 * kMaxStages + 4) * 8 + 64;
+
+int bn_max_of(int num_segments, const GemmSegment* segs) {
+  int m = 16;
+  for (int s = 0; s < num_segments; ++s) m = m > segs[s].bn ? m : segs[s].bn;
+  return m;
+}
+
 }  // namespace
 
-cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSegment* segs, const CUtensorMap* a0,
-                                const CUtensorMap* a1, const CUtensorMap* b, int num_sms, uint32_t* err,
-                                cudaStream_t stream) {
+// Largest number of 64-wide K blocks per pipeline stage (1, 2, 4; at most
+// MOE_KPS_MAX) that divides every segment's K slices and still leaves three
+// stages in shared memory.  Longer stages fetch longer contiguous runs of
+// each weight row per TMA request.
+#ifndef MOE_KPS_MAX
+#define MOE_KPS_MAX 2
+#endif
+int grouped_gemm_kps(GemmEpilogue epi, int num_segments, const GemmSegment* segs) {
+  const int num_a = (epi == kEpiSwiGLU) ? 2 : 1;
+  const int per_kb = num_a * kATileBytes + bn_max_of(num_segments, segs) * kTileK * 2;
+  int kps = 1;
+  for (int cand = 2; cand <= MOE_KPS_MAX; cand <<= 1) {
+    bool ok = (227 * 1024 - kFixedSmem) / (cand * per_kb) >= 3;
+    for (int s = 0; s < num_segments && ok; ++s) {
+      const int ks = (epi == kEpiSwiGLU || segs[s].ksplit < 1) ? 1 : segs[s].ksplit;
+      ok = segs[s].K % (kTileK * cand) == 0 && segs[s].K / (kTileK * cand) >= 2 * ks;
+    }
+    if (ok) kps = cand;
+  }
+  return kps;
+}
+
+cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSegment* segs, const SegMaps* seg_maps,
+                                int num_sms, uint32_t* err, cudaStream_t stream) {
   GemmArgs a{};
   a.nseg = num_segments;
   a.err = err;
   long long upper = 0;
   for (int s = 0; s < num_segments; ++s) {
     const GemmSegment& g = segs[s];
-    a.seg[s] = SegDev{g.offsets, g.groups, g.rows, g.nout, g.K, g.bn, g.ldo, g.out};
+    const int ks = (epi == kEpiSwiGLU || g.ksplit < 1) ? 1 : g.ksplit;
+    a.seg[s] = SegDev{g.offsets, g.groups, g.rows, g.nout, g.K, g.bn, g.ldo, ks, g.slice_stride, g.out};
     a.bn_max = a.bn_max > g.bn ? a.bn_max : g.bn;
-    upper += static_cast<long long>(g.nout / kTileM) * ((g.rows + g.bn - 1) / g.bn + g.groups);
+    upper += static_cast<long long>(g.nout / kTileM) * ((g.rows + g.bn - 1) / g.bn + g.groups) * ks;
   }
   const int num_a = (epi == kEpiSwiGLU) ? 2 : 1;
   a.acc_cols = num_a * a.bn_max;
   a.acc_stages = (2 * a.acc_cols <= 512) ? 2 : 1;
   a.tmem_cols = static_cast<int>(pow2_at_least(static_cast<uint32_t>(a.acc_stages * a.acc_cols)));
-  const int stage_bytes = num_a * kATileBytes + a.bn_max * kTileK * 2;
-  const int fixed = 1024 + kStagingBytes + static_cast<int>(sizeof(Sched)) + (2 * kMaxStages + 4) * 8 + 64;
+  a.kps = grouped_gemm_kps(epi, num_segments, segs);
+  const int stage_bytes = a.kps * (num_a * kATileBytes + a.bn_max * kTileK * 2);
+  const int fixed = kFixedSmem;
   int stages = (227 * 1024 - fixed) / stage_bytes;
   if (stages > kMaxStages) stages = kMaxStages;
   a.stages = stages;
@@ -382,8 +445,11 @@ cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSe
   int grid = num_sms;
   if (upper < grid) grid = static_cast<int>(upper);
   if (grid < 1) grid = 1;
-  if (epi == kEpiSwiGLU) return launch_epi<kEpiSwiGLU>(a, a0, a1, b, grid, smem, stream);
-  return launch_epi<kEpiStoreF32>(a, a0, a1, b, grid, smem, stream);
+  GemmMaps maps;
+  maps.seg[0] = seg_maps[0];
+  maps.seg[1] = seg_maps[num_segments > 1 ? 1 : 0];
+  if (epi == kEpiSwiGLU) return launch_epi<kEpiSwiGLU>(a, maps, grid, smem, stream);
+  return launch_epi<kEpiStoreF32>(a, maps, grid, smem, stream);
 }
 
 }  // namespace moe

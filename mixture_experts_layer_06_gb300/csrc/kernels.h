@@ -19,16 +19,25 @@ struct RouteSpec {
   const float* logit_bias;  // [E] or nullptr
 };
 
-// Router GEMM (x [T,H] . W_r[E,H]^T on the tensor cores) fused with the score
-// function and top-k.  map_x: box {64, 128}; map_wr: box {64, NE}, NE = E
-// rounded up to 16.
-cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_wr, int T, int H, int E, int k,
-                          const RouteSpec& spec, int32_t* topk_idx, float* topk_w, uint32_t* err,
-                          cudaStream_t stream);
+// Router launch plan: logit columns NE (E rounded up to 16, plus 16 when the
+// shared-expert gate vector rides along as one more B row), K slices and the
+// scratch (fp32 partial logits [ksplit][T][NE]) they need.  Shapes only.
+struct RouterPlan {
+  bool fused_gate;
+  int NE;
+  int ksplit;
+  int kb_per_split;
+  size_t scratch_bytes;
+};
+RouterPlan router_plan(int T, int H, int E, bool shared_gate);
 
-// shared_scale[t] = sigmoid(x[t] . w_s)
-cudaError_t launch_shared_gate(const void* x, const void* w_s, int T, int H, float* shared_scale,
-                               cudaStream_t stream);
+// Router GEMM (x [T,H] . [W_r; w_s]^T on the tensor cores, K-split) and the
+// per-token top-k.  map_x: box {64, 128}; map_wr: [E, H] box {64, E rounded up to 16};
+// map_ws: [1, H] box {64, 16} (used when the plan fuses the gate).
+cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_wr, const CUtensorMap* map_ws, int T,
+                          int H, int E, int k, const RouteSpec& spec, const void* x, const void* w_shared_gate,
+                          int32_t* topk_idx, float* topk_w, float* shared_scale, void* scratch, uint32_t* err,
+                          cudaStream_t stream);
 
 // Permutation: bitmap build, scan, gather (see permute.cu).
 size_t permute_scratch_bytes(int T, int E);
@@ -47,23 +56,40 @@ struct GemmSegment {
   int bn;                  // token tile (16, 32, 64, 128, 256)
   void* out;               // [rows, ldo] bf16 (SwiGLU) or fp32 (plain store)
   int ldo;
+  int ksplit = 1;          // plain store only: K cut into ksplit slices, slice s of
+                           // the partial sums goes to out + s * slice_stride
+  size_t slice_stride = 0; // elements
 };
 
 enum GemmEpilogue { kEpiSwiGLU = 0, kEpiStoreF32 = 1 };
 
-// Persistent grouped GEMM over one or two segments.  For segment s, A maps
-// are [groups*nout, K] weights with box {64, 128}; B map is [rows, K] with
-// box {64, bn}.  SwiGLU takes two A maps (gate, up) per segment.
+// K blocks (of 64) per pipeline stage the grouped GEMM will use for these
+// segments; A maps and the full-tile B map must have that box depth.
+int grouped_gemm_kps(GemmEpilogue epi, int num_segments, const GemmSegment* segs);
+
+// TMA descriptors of one grouped-GEMM segment.  a0 / a1 cover the
+// [groups*nout, K] weights (gate and up for SwiGLU; a1 unused otherwise) with
+// box 128 rows x 64 columns; b covers the [rows, K] token rows with box bn
+// rows x 64 columns.  With kps > 1 they are 3-D views {64, rows, K/64} with
+// box depth kps.
+struct SegMaps {
+  CUtensorMap a0, a1, b;
+};
+
+// Persistent grouped GEMM over one or two segments (seg_maps[s] for segment s).
 cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSegment* segs,
-                                const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* b,
-                                int num_sms, uint32_t* err, cudaStream_t stream);
+                                const SegMaps* seg_maps, int num_sms, uint32_t* err, cudaStream_t stream);
 
 // Address of the current device's error word (nullptr if the device could
 // not be set up).
 uint32_t* device_error_word();
 
-// Deterministic weighted combine.
+// Deterministic weighted combine.  y_perm (and y_shared) may hold nslices
+// partial-sum slices slice_stride elements apart; they are added in slice
+// order before weighting.
 cudaError_t launch_combine(const float* y_perm, const int32_t* inv, const float* topk_w, const float* y_shared,
-                           const float* shared_scale, int T, int H, int k, void* out, cudaStream_t stream);
+                           const float* shared_scale, int T, int H, int k, void* out, cudaStream_t stream,
+                           int nslices = 1, size_t slice_stride = 0, int nslices_shared = 1,
+                           size_t slice_stride_shared = 0);
 
 }  // namespace moe

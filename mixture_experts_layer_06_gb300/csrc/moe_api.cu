@@ -96,6 +96,26 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view {64, rows, cols/64} of a bf16 [rows, cols] row-major matrix, box
+// {64, box_rows, box_k}: one request brings box_k consecutive 64-column
+// blocks of box_rows rows, each block landing as its own 128-byte-swizzled
+// tile.
+bool make_map3d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_k) {
+  const cuuint64_t dims[3] = {64, rows, cols / 64};
+  const cuuint64_t strides[2] = {cols * 2, 128};
+  const cuuint32_t box[3] = {64, box_rows, box_k};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Weight / token-row map for the grouped GEMM: 2-D for one K block per
+// stage, 3-D with box depth kps otherwise.
+bool make_gemm_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows, int kps) {
+  return kps == 1 ? make_map(m, base, rows, cols, box_rows) : make_map3d(m, base, rows, cols, box_rows, kps);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 moe_status_t check_dims(int T, int H, int F, int E, int k) {
@@ -153,9 +173,46 @@ int choose_bn(long long rows, int groups, int bn_max = 256) {
   return bn;
 }
 
+// Router scratch: fp32 partial logits of the K-split router GEMM.
+size_t route_scratch(const moe_config_t& c, int T, int H, int E) {
+  return moe::router_plan(T, H, E, c.w_shared_gate != nullptr).scratch_bytes;
+}
+
+// K-split of the down projection in moe_forward_ex.  When the routed rows
+// give too few output tiles to fill the GPU several times over (small T:
+// few active experts and one token tile each), K (= F) is cut into
+// 2, 4 or 8 slices whose fp32 partial sums go to separate y slices; the
+// combine adds them in slice order, so the result stays deterministic.  The
+// shared expert's K (= F_shared) is cut so that its slices are no longer
+// than the routed ones.  Depends only on the shapes (not on the device), so
+// that moe_workspace_bytes() can size the slices.
+constexpr long long kTargetTiles = 6 * 152;
+
+struct Split {
+  int routed = 1, shared = 1;
+};
+
+Split choose_split(const moe_config_t& c, int T, int H, int F, int E, int k) {
+  Split sp;
+  const long long Tk = static_cast<long long>(T) * k;
+  const long long groups = Tk < E ? Tk : E;
+  if (groups <= 0) return sp;
+  const long long rows_per = (Tk + groups - 1) / groups;
+  const int bn = choose_bn(Tk, E);
+  const long long tiles = groups * (H / 128) * ((rows_per + bn - 1) / bn);
+  const int kb = F / 64;
+  while (sp.routed < 8 && tiles * sp.routed < kTargetTiles && kb / (2 * sp.routed) >= 8) sp.routed <<= 1;
+  if (c.F_shared > 0) {
+    const long long slice = F / sp.routed;
+    const int kbs = c.F_shared / 64;
+    while (sp.shared < 8 && c.F_shared / sp.shared > slice && kbs / (2 * sp.shared) >= 8) sp.shared <<= 1;
+  }
+  return sp;
+}
+
 // Workspace carve-up of moe_forward_ex, 256-byte aligned pieces.
 struct Layout {
-  size_t topk_idx, topk_w, shared_scale, counts, offsets, perm, inv, scratch, x_perm, h_perm, y_perm, h_shared,
+  size_t route_scratch, topk_idx, topk_w, shared_scale, counts, offsets, perm, inv, scratch, x_perm, h_perm, y_perm, h_shared,
       y_shared, total;
 };
 
@@ -170,6 +227,7 @@ Layout layout(const moe_config_t& c, int T, int H, int F, int E, int k) {
     o += up256(bytes);
     return at;
   };
+  L.route_scratch = take(route_scratch(c, T, H, E));
   L.topk_idx = take(Tk * 4);
   L.topk_w = take(Tk * 4);
   L.shared_scale = take(static_cast<size_t>(T) * 4);
@@ -180,26 +238,26 @@ Layout layout(const moe_config_t& c, int T, int H, int F, int E, int k) {
   L.scratch = take(moe::permute_scratch_bytes(T, E));
   L.x_perm = take(Tk * H * 2);
   L.h_perm = take(Tk * F * 2);
-  L.y_perm = take(Tk * H * 4);
+  const Split sp = choose_split(c, T, H, F, E, k);
+  L.y_perm = take(sp.routed * Tk * H * 4);
   const size_t Fs = c.F_shared > 0 ? static_cast<size_t>(c.F_shared) : 0;
   L.h_shared = take(static_cast<size_t>(T) * Fs * 2);
-  L.y_shared = take(Fs ? static_cast<size_t>(T) * H * 4 : 0);
+  L.y_shared = take(Fs ? sp.shared * static_cast<size_t>(T) * H * 4 : 0);
   L.total = o;
   return L;
 }
 
 moe_status_t route_impl(DeviceState* d, const moe_config_t& c, const void* x, const void* w_router, int T, int H,
-                        int E, int k, int32_t* topk_idx, float* topk_w, float* shared_scale, cudaStream_t stream) {
-  CUtensorMap mx, mw;
-  const uint32_t ne = static_cast<uint32_t>((E + 15) / 16 * 16);
-  if (!make_map(&mx, x, T, H, 128) || !make_map(&mw, w_router, E, H, ne)) return MOE_ERR_CUDA;
-  cudaError_t e = moe::launch_router(mx, mw, T, H, E, k, route_spec(c), topk_idx, topk_w, d->err, stream);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  if (c.w_shared_gate != nullptr && shared_scale != nullptr) {
-    e = moe::launch_shared_gate(x, c.w_shared_gate, T, H, shared_scale, stream);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-  }
-  return MOE_OK;
+                        int E, int k, int32_t* topk_idx, float* topk_w, float* shared_scale, void* scratch,
+                        cudaStream_t stream) {
+  CUtensorMap mx, mw, ms;
+  if (!make_map(&mx, x, T, H, 128) || !make_map(&mw, w_router, E, H, (E + 15) / 16 * 16)) return MOE_ERR_CUDA;
+  const bool gate = c.w_shared_gate != nullptr && shared_scale != nullptr;
+  if (gate && !make_map(&ms, c.w_shared_gate, 1, H, 16)) return MOE_ERR_CUDA;
+  const cudaError_t e = moe::launch_router(mx, mw, gate ? &ms : nullptr, T, H, E, k, route_spec(c), x,
+                                           gate ? c.w_shared_gate : nullptr, topk_idx, topk_w,
+                                           gate ? shared_scale : nullptr, scratch, d->err, stream);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status_t permute_impl(DeviceState* d, const int32_t* topk_idx, const void* x, int T, int H, int E, int k,
@@ -223,33 +281,46 @@ struct FfnOperands {
   const void *w_gate, *w_up, *w_down;
   void* h;
   float* y;
+  int ksplit = 1;  // down projection K slices (y holds ksplit slices of rows*H)
 };
 
 moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStream_t stream, bool traced = false) {
-  CUtensorMap a0[2], a1[2], b[2];
+  moe::SegMaps maps[2];
   GemmSegment seg[2];
+  // gate+up: B = token rows [rows, H], A = gate / up weights [groups*F, H]
   for (int s = 0; s < nseg; ++s) {
     const FfnOperands& o = ops[s];
-    const int bn = choose_bn(o.rows, o.groups, MOE_SWIGLU_BN_MAX);
-    const uint64_t wrows = static_cast<uint64_t>(o.groups) * o.F;
-    if (!make_map(&a0[s], o.w_gate, wrows, o.H, 128) || !make_map(&a1[s], o.w_up, wrows, o.H, 128) ||
-        !make_map(&b[s], o.x_rows, o.rows, o.H, bn))
-      return MOE_ERR_CUDA;
-    seg[s] = GemmSegment{o.offsets, o.groups, o.rows, o.F, o.H, bn, o.h, o.F};
+    seg[s] = GemmSegment{o.offsets, o.groups, o.rows, o.F, o.H, choose_bn(o.rows, o.groups, MOE_SWIGLU_BN_MAX),
+                         o.h, o.F};
   }
-  if (moe::launch_grouped_gemm(moe::kEpiSwiGLU, nseg, seg, a0, a1, b, d->num_sms, d->err, stream) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  int kps = moe::grouped_gemm_kps(moe::kEpiSwiGLU, nseg, seg);
   for (int s = 0; s < nseg; ++s) {
     const FfnOperands& o = ops[s];
-    const int bn = choose_bn(o.rows, o.groups);
+    const uint64_t wrows = static_cast<uint64_t>(o.groups) * o.F;
+    if (!make_gemm_map(&maps[s].a0, o.w_gate, wrows, o.H, 128, kps) ||
+        !make_gemm_map(&maps[s].a1, o.w_up, wrows, o.H, 128, kps) ||
+        !make_gemm_map(&maps[s].b, o.x_rows, o.rows, o.H, seg[s].bn, kps))
+      return MOE_ERR_CUDA;
+  }
+  if (moe::launch_grouped_gemm(moe::kEpiSwiGLU, nseg, seg, maps, d->num_sms, d->err, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  // down: B = h [rows, F], A = down weights [groups*H, F]
+  for (int s = 0; s < nseg; ++s) {
+    const FfnOperands& o = ops[s];
+    seg[s] = GemmSegment{o.offsets, o.groups, o.rows, o.H, o.F, choose_bn(o.rows, o.groups), o.y, o.H, o.ksplit,
+                         static_cast<size_t>(o.rows) * o.H};
+  }
+  kps = moe::grouped_gemm_kps(moe::kEpiStoreF32, nseg, seg);
+  for (int s = 0; s < nseg; ++s) {
+    const FfnOperands& o = ops[s];
     const uint64_t wrows = static_cast<uint64_t>(o.groups) * o.H;
-    if (!make_map(&a0[s], o.w_down, wrows, o.F, 128) || !make_map(&b[s], o.h, o.rows, o.F, bn)) return MOE_ERR_CUDA;
-    a1[s] = a0[s];
-    seg[s] = GemmSegment{o.offsets, o.groups, o.rows, o.H, o.F, bn, o.y, o.H};
+    if (!make_gemm_map(&maps[s].a0, o.w_down, wrows, o.F, 128, kps) ||
+        !make_gemm_map(&maps[s].b, o.h, o.rows, o.F, seg[s].bn, kps))
+      return MOE_ERR_CUDA;
+    maps[s].a1 = maps[s].a0;
   }
   if (traced) trace(3, stream);
-  if (moe::launch_grouped_gemm(moe::kEpiStoreF32, nseg, seg, a0, a1, b, d->num_sms, d->err, stream) !=
-      cudaSuccess)
+  if (moe::launch_grouped_gemm(moe::kEpiStoreF32, nseg, seg, maps, d->num_sms, d->err, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -305,8 +376,19 @@ const char* moe_status_string(moe_status_t s) {
   return "MOE_ERR_UNKNOWN";
 }
 
+size_t moe_route_scratch_bytes(const moe_config_t* cfg, int T, int H, int E) {
+  moe_config_t c;
+  if (cfg)
+    c = *cfg;
+  else
+    moe_config_default(&c);
+  if (T < 0 || H <= 0 || H % 128 != 0 || E <= 0 || E > 256) return 0;
+  return route_scratch(c, T, H, E);
+}
+
 moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_router, int T, int H, int E, int k,
-                       int32_t* topk_idx, float* topk_w, float* shared_scale, moe_stream_t stream) {
+                       int32_t* topk_idx, float* topk_w, float* shared_scale, void* scratch, size_t scratch_bytes,
+                       moe_stream_t stream) {
   moe_config_t c;
   if (cfg)
     c = *cfg;
@@ -319,9 +401,11 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_rou
   if (c.w_shared_gate && !shared_scale) return MOE_ERR_INVALID_VALUE;
   if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_VALUE;
   if (T == 0) return MOE_OK;
+  if (!scratch || !aligned16(scratch)) return MOE_ERR_INVALID_VALUE;
+  if (scratch_bytes < route_scratch(c, T, H, E)) return MOE_ERR_WORKSPACE;
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != MOE_OK) return st;
-  return route_impl(d, c, x, w_router, T, H, E, k, topk_idx, topk_w, shared_scale,
+  return route_impl(d, c, x, w_router, T, H, E, k, topk_idx, topk_w, shared_scale, scratch,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -414,26 +498,31 @@ moe_status_t moe_forward_ex(const moe_config_t* cfg, const void* x, const void* 
   const int Tk = T * k;
 
   trace(0, s);
-  if ((st = route_impl(d, c, x, w_router, T, H, E, k, topk_idx, topk_w, shared_scale, s)) != MOE_OK) return st;
+  if ((st = route_impl(d, c, x, w_router, T, H, E, k, topk_idx, topk_w, shared_scale, at(L.route_scratch), s)) !=
+      MOE_OK)
+    return st;
   trace(1, s);
   if ((st = permute_impl(d, topk_idx, x, T, H, E, k, static_cast<int32_t*>(at(L.counts)), offsets,
                          static_cast<int32_t*>(at(L.perm)), inv, at(L.x_perm), at(L.scratch), s)) != MOE_OK)
     return st;
+  const Split sp = choose_split(c, T, H, F, E, k);
   FfnOperands ops[2];
   ops[0] = FfnOperands{at(L.x_perm), offsets, Tk, E, H, F, w_gate, w_up, w_down, at(L.h_perm),
-                       static_cast<float*>(at(L.y_perm))};
+                       static_cast<float*>(at(L.y_perm)), sp.routed};
   int nseg = 1;
   float* y_shared = nullptr;
   if (c.F_shared > 0) {
     y_shared = static_cast<float*>(at(L.y_shared));
-    ops[1] = FfnOperands{x, nullptr, T, 1, H, c.F_shared, c.ws_gate, c.ws_up, c.ws_down, at(L.h_shared), y_shared};
+    ops[1] = FfnOperands{x, nullptr, T, 1, H, c.F_shared, c.ws_gate, c.ws_up, c.ws_down, at(L.h_shared), y_shared,
+                         sp.shared};
     nseg = 2;
   }
   trace(2, s);
   if ((st = ffn_impl(d, nseg, ops, s, true)) != MOE_OK) return st;
   trace(4, s);
   st = cuda_status(moe::launch_combine(static_cast<float*>(at(L.y_perm)), inv, topk_w, y_shared, shared_scale, T,
-                                       H, k, out, s));
+                                       H, k, out, s, sp.routed, static_cast<size_t>(Tk) * H, sp.shared,
+                                       static_cast<size_t>(T) * H));
   trace(5, s);
   return st;
 }

@@ -104,6 +104,9 @@ __global__ void __launch_bounds__(1024, 1)
   }
 }
 
+// Grid (token blocks of 8, chunks of 256 columns): warp = (token, chunk).
+// Every warp computes its token's k grouped rows; the chunk-0 warp writes
+// perm / inv; each warp copies its 512-byte piece of x[t] to the k rows.
 __global__ void gather_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int T, int H8, int E,
                               int k, const uint32_t* __restrict__ bitmap, const uint32_t* __restrict__ rowbase,
                               int32_t* __restrict__ perm, int32_t* __restrict__ inv, uint4* __restrict__ x_perm,
@@ -118,20 +121,22 @@ __global__ void gather_kernel(const int32_t* __restrict__ idx, const uint4* __re
       const size_t we = static_cast<size_t>(t >> 5) * E + e;
       r = static_cast<int>(rowbase[we] + __popc(bitmap[we] & ((1u << (t & 31)) - 1u)));
       if (r >= rows) {
-        raise_error(err, kErrBounds, kSitePermuteIndex);
+        if (blockIdx.y == 0) raise_error(err, kErrBounds, kSitePermuteIndex);
         r = -1;
       }
     }
-    if (r >= 0) perm[r] = t * k + lane;
-    inv[static_cast<size_t>(t) * k + lane] = r;
-  }
-  const uint4* src = x + static_cast<size_t>(t) * H8;
-  for (int v = lane; v < H8; v += 32) {
-    const uint4 val = src[v];
-    for (int j = 0; j < k; ++j) {
-      const int rj = __shfl_sync(0xFFFFFFFFu, r, j);
-      if (rj >= 0) x_perm[static_cast<size_t>(rj) * H8 + v] = val;
+    if (blockIdx.y == 0) {
+      if (r >= 0) perm[r] = t * k + lane;
+      inv[static_cast<size_t>(t) * k + lane] = r;
     }
+  }
+  const int v = blockIdx.y * 32 + lane;
+  const bool active = v < H8;
+  uint4 val = make_uint4(0, 0, 0, 0);
+  if (active) val = x[static_cast<size_t>(t) * H8 + v];
+  for (int j = 0; j < k; ++j) {
+    const int rj = __shfl_sync(0xFFFFFFFFu, r, j);  // all lanes take part
+    if (active && rj >= 0) x_perm[static_cast<size_t>(rj) * H8 + v] = val;
   }
 }
 
@@ -152,7 +157,8 @@ cudaError_t launch_permute(const int32_t* topk_idx, const void* x, int T, int H,
   bitmap_kernel<<<(W + kWarpsPerBlock - 1) / kWarpsPerBlock, threads, 0, stream>>>(topk_idx, T, E, k, W, bitmap,
                                                                                  err);
   scan_kernel<<<1, 1024, 0, stream>>>(bitmap, W, E, counts, offsets, rowbase);
-  gather_kernel<<<(T + kWarpsPerBlock - 1) / kWarpsPerBlock, threads, 0, stream>>>(
+  const dim3 ggrid((T + kWarpsPerBlock - 1) / kWarpsPerBlock, (H / 8 + 31) / 32);
+  gather_kernel<<<ggrid, threads, 0, stream>>>(
       topk_idx, static_cast<const uint4*>(x), T, H / 8, E, k, bitmap, rowbase, perm, inv,
       static_cast<uint4*>(x_perm), err);
   return cudaGetLastError();

@@ -1,14 +1,22 @@
 // Router scoring + top-k selection.
 //
 // "Cross-Platform Fused MoE Dispatch in Triton" (review page), "The reading":
-// every token is first scored by the router.  Here the scoring GEMM
-// logits[T, E] = x[T, H] . W_r[E, H]^T runs on the 5th-generation tensor
-// cores (tcgen05.mma, operands staged by TMA, fp32 accumulator in TMEM), and
-// the epilogue reads each token's E logits straight out of its TMEM lane:
-// one thread per token applies the logit bias, the score function (softmax or
-// sigmoid), optional group limiting, and keeps the k best experts in
-// registers.  Nothing but topk_idx / topk_w is written to global memory.
+// every token is first scored by the router; "Assumptions & free parameters":
+// the standard softmax/sigmoid router with top-k selection.
+//
+// Two launches:
+//  1. router_gemm_kernel: logits = x . [W_r; w_s]^T on the 5th-generation
+//     tensor cores (tcgen05.mma, operands staged by TMA, fp32 accumulator in
+//     TMEM).  The grid is (token tiles of 128) x (K slices), so that even a
+//     single token spreads the W_r stream over many SMs; each CTA writes its
+//     fp32 partial logits to a slice of the scratch.  With a sigmoid-gated
+//     shared expert the gate vector w_s rides along as one more B row.
+//  2. router_topk_kernel: one warp per token adds the K-slice partials in
+//     slice order, applies the logit bias and the score function, optional
+//     group limiting, and picks the k best experts by warp-wide arg-max
+//     rounds (ties to the lower expert index).  Deterministic.
 #include <cfloat>
+#include <climits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -21,196 +29,42 @@ constexpr int kMaxStages = 8;
 constexpr int kTileM = 128;    // tokens per CTA
 constexpr int kTileK = 64;     // bf16 elements per 128-byte swizzled row
 constexpr int kATileBytes = kTileM * kTileK * 2;
+constexpr int kBoxBytes = 16 * kTileK * 2;  // one 16-row box of B rows
+constexpr int kJMax = 8;                    // logit columns per lane in the top-k kernel (<= 256 columns)
 
-struct RouterArgs {
-  int T, H, E, k, NE, stages, tmem_cols;
-  RouteSpec spec;
-  int32_t* topk_idx;
-  float* topk_w;
+struct GemmArgs {
+  int T, H, NE, n_wr_boxes, gate_box, stages, tmem_cols, kb_per_split;
+  float* partial;  // [ksplit][T][NE]
   uint32_t* err;
 };
 
-// Keep the KMAX largest values seen so far, sorted descending; a value equal
-// to one already kept goes after it (so earlier = lower index wins ties).
-template <int KMAX>
-__device__ __forceinline__ void keep_top(float (&bv)[KMAX], int (&bi)[KMAX], float v, int e) {
-#pragma unroll
-  for (int j = KMAX - 1; j >= 0; --j) {
-    if (v > bv[j]) {
-      if (j > 0 && v > bv[j - 1]) {
-        bv[j] = bv[j - 1];
-        bi[j] = bi[j - 1];
-      } else {
-        bv[j] = v;
-        bi[j] = e;
-      }
-    }
-  }
-}
-
-// Load TMEM columns [c0, c0+32) (or 16 when only 16 remain) of this warp's lanes.
-__device__ __forceinline__ void load_chunk(uint32_t taddr, int remaining, uint32_t (&r)[32]) {
-  if (remaining >= 32)
-    tmem_ld32(taddr, r);
-  else
-    tmem_ld16(taddr, r);
-  tmem_wait(r);
-}
-
-template <int KMAX>
-__device__ void router_epilogue(const RouterArgs& a, uint32_t tmem_base, const float* bias_s, int m0) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q = warp & 3;  // TMEM lane quarter this warp may access
-  const int row = m0 + q * 32 + lane;
-  const uint32_t tbase = tmem_addr(tmem_base, q * 32, 0);
-  const int E = a.E, NE = a.NE;
-  const bool sigmoid = a.spec.sigmoid != 0;
-
-  // Pass 1: max and sum of exp over all E logits (softmax normaliser).
-  float mx = -FLT_MAX, se = 0.f;
-  for (int c0 = 0; c0 < NE; c0 += 32) {
-    uint32_t r[32];
-    load_chunk(tbase + c0, NE - c0, r);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = c0 + i;
-      if (e < E) {
-        const float l = __uint_as_float(r[i]) + bias_s[e];
-        if (l > mx) {
-          se = se * __expf(mx - l) + 1.f;
-          mx = l;
-        } else {
-          se += __expf(l - mx);
-        }
-      }
-    }
-  }
-  const float inv_se = 1.f / se;
-
-  // Pass 2 (group-limited routing): group scores and the kept-group mask.
-  uint32_t kept = 0xFFFFFFFFu;
-  int gsize = E;
-  if (a.spec.n_group > 1) {
-    gsize = E / a.spec.n_group;
-    float gsc[16];
-    float top[4] = {-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX};
-    int topi[4] = {0, 0, 0, 0};
-    int g = 0, gi = 0;
-    for (int c0 = 0; c0 < NE; c0 += 32) {
-      uint32_t r[32];
-      load_chunk(tbase + c0, NE - c0, r);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int e = c0 + i;
-        if (e < E) {
-          const float l = __uint_as_float(r[i]) + bias_s[e];
-          const float sc = sigmoid ? 1.f / (1.f + __expf(-l)) : __expf(l - mx) * inv_se;
-          keep_top<4>(top, topi, sc, e);
-          if (++gi == gsize) {
-            float sum = 0.f;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (j < a.spec.group_topn) sum += top[j];
-            gsc[g++] = sum;
-            gi = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) top[j] = -FLT_MAX;
-          }
-        }
-      }
-    }
-    kept = 0;
-    for (int rsel = 0; rsel < a.spec.topk_group; ++rsel) {
-      int best = -1;
-      float bestv = -FLT_MAX;
-      for (int gg = 0; gg < a.spec.n_group; ++gg) {
-        if ((kept >> gg) & 1u) continue;
-        if (best < 0 || gsc[gg] > bestv) {
-          best = gg;
-          bestv = gsc[gg];
-        }
-      }
-      kept |= 1u << best;
-    }
-  }
-
-  // Pass 3: the KMAX best candidate logits (score functions are monotone).
-  float bv[KMAX];
-  int bi[KMAX];
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j) {
-    bv[j] = -FLT_MAX;
-    bi[j] = 0;
-  }
-  {
-    int g = 0, gi = 0;
-    for (int c0 = 0; c0 < NE; c0 += 32) {
-      uint32_t r[32];
-      load_chunk(tbase + c0, NE - c0, r);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int e = c0 + i;
-        if (e < E) {
-          if ((kept >> g) & 1u) keep_top<KMAX>(bv, bi, __uint_as_float(r[i]) + bias_s[e], e);
-          if (++gi == gsize) {
-            gi = 0;
-            ++g;
-          }
-        }
-      }
-    }
-  }
-
-  if (row < a.T) {
-    float sc[KMAX];
-    float sum = 0.f;
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      sc[j] = sigmoid ? 1.f / (1.f + __expf(-bv[j])) : __expf(bv[j] - mx) * inv_se;
-      if (j < a.k) sum += sc[j];
-    }
-    const float scale = a.spec.renormalize ? a.spec.route_scale / sum : a.spec.route_scale;
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      if (j < a.k) {
-        a.topk_idx[static_cast<size_t>(row) * a.k + j] = bi[j];
-        a.topk_w[static_cast<size_t>(row) * a.k + j] = sc[j] * scale;
-      }
-    }
-  }
-}
-
-template <int KMAX>
 __global__ void __launch_bounds__(kThreads, 1)
-    router_topk_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_wr,
-                       const RouterArgs a) {
+    router_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_wr,
+                       const __grid_constant__ CUtensorMap map_ws, const GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages;
-  const int b_tile_bytes = a.NE * kTileK * 2;
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + S * kATileBytes;
-  float* bias_s = reinterpret_cast<float*>(sB + S * b_tile_bytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(bias_s + 256);
+  const int stage_bytes = kATileBytes + a.NE * kTileK * 2;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * stage_bytes);
   uint64_t* empty = full + kMaxStages;
   uint64_t* acc_full = empty + kMaxStages;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * kTileM;
+  const int ks = blockIdx.y;
   const int KB = a.H / kTileK;
+  const int kb0 = ks * a.kb_per_split;
+  const int kb1 = min(KB, kb0 + a.kb_per_split);
+  const int nboxes = a.n_wr_boxes + (a.gate_box >= 0 ? 1 : 0);
 
-  for (int e = threadIdx.x; e < 256; e += kThreads)
-    bias_s[e] = (a.spec.logit_bias != nullptr && e < a.E) ? a.spec.logit_bias[e] : 0.f;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 64) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
     fence_mbar_init();
-    tma_prefetch_map(&map_x);
-    tma_prefetch_map(&map_wr);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, a.tmem_cols);
@@ -222,48 +76,67 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_holder;
 
   if (warp == 0) {
+    // Lane 0: wait for the slot, post the bytes, load the x tile, the W_r rows
+    // (one box) and, with a fused gate, the w_s row (one 16-row box).
     if (lane == 0) {
-      const uint32_t bytes = kATileBytes + b_tile_bytes;
       int issued = 0;
-      for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % S;
-        const uint32_t ph = (kb / S) & 1;
+      for (int kb = kb0; kb < kb1; ++kb, ++issued) {
+        const int s = issued % S;
+        const uint32_t ph = (issued / S) & 1;
         if (!mbar_wait(&empty[s], ph ^ 1, a.err, kSiteRouterProducer)) break;
-        mbar_arrive_expect_tx(&full[s], bytes);
-        tma_load_2d(sA + s * kATileBytes, &map_x, &full[s], kb * kTileK, m0);
-        tma_load_2d(sB + s * b_tile_bytes, &map_wr, &full[s], kb * kTileK, 0);
-        ++issued;
+        mbar_arrive_expect_tx(&full[s], kATileBytes + nboxes * kBoxBytes);
+        uint8_t* st = smem + s * stage_bytes;
+        tma_load_2d(st, &map_x, &full[s], kb * kTileK, m0);
+        tma_load_2d(st + kATileBytes, &map_wr, &full[s], kb * kTileK, 0);
+        if (a.gate_box >= 0) tma_load_2d(st + kATileBytes + a.gate_box * kBoxBytes, &map_ws, &full[s], kb * kTileK, 0);
       }
       // Do not leave while copies into this CTA's shared memory are in flight.
-      for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
-        mbar_wait(&full[kb % S], (kb / S) & 1, a.err, kSiteTeardown);
+      for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
+        mbar_wait(&full[i % S], (i / S) & 1, a.err, kSiteTeardown);
     }
+    __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kTileM, a.NE);
-      bool ok = true;
-      for (int kb = 0; kb < KB && ok; ++kb) {
-        const int s = kb % S;
-        const uint32_t ph = (kb / S) & 1;
-        if (!mbar_wait(&full[s], ph, a.err, kSiteRouterMma)) {
-          ok = false;
-          break;
-        }
+      int n = 0;
+      for (int kb = kb0; kb < kb1; ++kb, ++n) {
+        const int s = n % S;
+        if (!mbar_wait(&full[s], (n / S) & 1, a.err, kSiteRouterMma)) break;
         tc_fence_after_sync();
-        const uint32_t a_addr = smem_u32(sA + s * kATileBytes);
-        const uint32_t b_addr = smem_u32(sB + s * b_tile_bytes);
+        const uint32_t a_addr = smem_u32(smem + s * stage_bytes);
+        const uint32_t b_addr = a_addr + kATileBytes;
 #pragma unroll
         for (int kk = 0; kk < kTileK / 16; ++kk)
           umma_bf16(tmem_base, sdesc_k128(a_addr + kk * 32), sdesc_k128(b_addr + kk * 32), idesc,
-                    (kb | kk) != 0);
+                    (kb != kb0 || kk != 0));
         umma_commit(&empty[s]);
       }
       umma_commit(acc_full);
     }
   } else {
+    // Epilogue: thread = token row (TMEM lane); write its NE partial logits.
     if (mbar_wait(acc_full, 0, a.err, kSiteRouterEpilogue)) {
       tc_fence_after_sync();
-      router_epilogue<KMAX>(a, tmem_base, bias_s, m0);
+      const int q = warp & 3;
+      const int row = m0 + q * 32 + lane;
+      float* dst = a.partial + (static_cast<size_t>(ks) * a.T + row) * a.NE;
+      for (int c0 = 0; c0 < a.NE; c0 += 32) {
+        uint32_t r[32];
+        const uint32_t ta = tmem_addr(tmem_base, q * 32, c0);
+        if (a.NE - c0 >= 32)
+          tmem_ld32(ta, r);
+        else
+          tmem_ld16(ta, r);
+        tmem_wait(r);
+        const int nc = min(32, a.NE - c0);
+        if (row < a.T) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            if (i < nc)
+              *reinterpret_cast<float4*>(dst + c0 + i) = make_float4(
+                  __uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+        }
+      }
     }
     tc_fence_before_sync();
   }
@@ -275,7 +148,142 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Warp-wide arg-max: the larger value wins, equal values go to the lower index.
+__device__ __forceinline__ void warp_best(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float v2 = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    const int i2 = __shfl_xor_sync(0xFFFFFFFFu, i, o);
+    if (v2 > v || (v2 == v && i2 < i)) {
+      v = v2;
+      i = i2;
+    }
+  }
+}
+
+struct TopkArgs {
+  const float* partial;
+  int ksplit, T, NE, E, k, gate_col;
+  RouteSpec spec;
+  int32_t* topk_idx;
+  float* topk_w;
+  float* shared_scale;
+};
+
+__global__ void router_topk_kernel(const TopkArgs a) {
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= a.T) return;  // warp-uniform
+  const int E = a.E;
+  const bool sigmoid = a.spec.sigmoid != 0;
+
+  // Logit column c = lane + 32 j lives in l[j]; partials added in slice order.
+  float l[kJMax];
+#pragma unroll
+  for (int j = 0; j < kJMax; ++j) {
+    const int c = lane + 32 * j;
+    float v = -INFINITY;
+    if (c < a.NE) {
+      v = 0.f;
+      for (int s = 0; s < a.ksplit; ++s) v += a.partial[(static_cast<size_t>(s) * a.T + t) * a.NE + c];
+      if (c == a.gate_col) a.shared_scale[t] = 1.f / (1.f + __expf(-v));
+      if (c < E) {
+        if (a.spec.logit_bias != nullptr) v += a.spec.logit_bias[c];
+      } else {
+        v = -INFINITY;
+      }
+    }
+    l[j] = v;
+  }
+
+  // Softmax normaliser over all E logits (fixed butterfly order).
+  float mx = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kJMax; ++j) mx = fmaxf(mx, l[j]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  float se = 0.f;
+#pragma unroll
+  for (int j = 0; j < kJMax; ++j)
+    if (lane + 32 * j < E) se += __expf(l[j] - mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) se += __shfl_xor_sync(0xFFFFFFFFu, se, o);
+  const float inv_se = 1.f / se;
+  auto score = [&](float v) { return sigmoid ? 1.f / (1.f + __expf(-v)) : __expf(v - mx) * inv_se; };
+
+  // Group limiting: group score = sum of its top group_topn scores; keep the
+  // topk_group best groups (lane g holds group g's score).
+  const int gsize = a.spec.n_group > 1 ? E / a.spec.n_group : E;
+  uint32_t kept = 0xFFFFFFFFu;
+  if (a.spec.n_group > 1) {
+    float my_gscore = -INFINITY;
+    for (int g = 0; g < a.spec.n_group; ++g) {
+      uint32_t taken = 0;
+      float sum = 0.f;
+      for (int r = 0; r < a.spec.group_topn; ++r) {
+        float v = -INFINITY;
+        int i = INT_MAX;
+#pragma unroll
+        for (int j = 0; j < kJMax; ++j) {
+          const int c = lane + 32 * j;
+          if (c < E && c / gsize == g && !((taken >> j) & 1u)) {
+            const float sc = score(l[j]);
+            if (sc > v || (sc == v && c < i)) {
+              v = sc;
+              i = c;
+            }
+          }
+        }
+        warp_best(v, i);
+        sum += v;
+        if (i != INT_MAX && (i & 31) == lane) taken |= 1u << (i >> 5);
+      }
+      if (lane == g) my_gscore = sum;
+    }
+    kept = 0;
+    for (int r = 0; r < a.spec.topk_group; ++r) {
+      float v = (lane < a.spec.n_group && !((kept >> lane) & 1u)) ? my_gscore : -INFINITY;
+      int i = lane < a.spec.n_group ? lane : INT_MAX;
+      warp_best(v, i);
+      if (i != INT_MAX) kept |= 1u << i;
+    }
+  }
+
+  // k rounds of warp arg-max over the candidate logits (the score functions
+  // are monotone, so ordering by logit is ordering by score).
+  uint32_t taken = 0;
+  int my_idx = 0;
+  float my_score = 0.f, sum = 0.f;
+  for (int r = 0; r < a.k; ++r) {
+    float v = -INFINITY;
+    int i = INT_MAX;
+#pragma unroll
+    for (int j = 0; j < kJMax; ++j) {
+      const int c = lane + 32 * j;
+      if (c < E && ((kept >> (c / gsize)) & 1u) && !((taken >> j) & 1u)) {
+        if (l[j] > v || (l[j] == v && c < i)) {
+          v = l[j];
+          i = c;
+        }
+      }
+    }
+    warp_best(v, i);
+    if (i != INT_MAX && (i & 31) == lane) taken |= 1u << (i >> 5);
+    const float sc = score(v);
+    sum += sc;
+    if (lane == r) {
+      my_idx = i;
+      my_score = sc;
+    }
+  }
+  if (lane < a.k) {
+    const float scale = a.spec.renormalize ? a.spec.route_scale / sum : a.spec.route_scale;
+    a.topk_idx[static_cast<size_t>(t) * a.k + lane] = my_idx;
+    a.topk_w[static_cast<size_t>(t) * a.k + lane] = my_score * scale;
+  }
+}
+
 // shared_scale[t] = sigmoid(x[t] . w_s): one warp per token, 16-byte loads.
+// Used only when the gate vector does not fit as an extra router B row.
 __global__ void shared_gate_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ ws, int T,
                                    int H, float* __restrict__ scale) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
@@ -299,59 +307,82 @@ __global__ void shared_gate_kernel(const __nv_bfloat16* __restrict__ x, const __
   if (lane == 0) scale[warp] = 1.f / (1.f + __expf(-acc));
 }
 
-template <int KMAX>
-cudaError_t launch_router_k(const CUtensorMap& mx, const CUtensorMap& mw, const RouterArgs& a, size_t smem,
-                            cudaStream_t stream) {
+}  // namespace
+
+RouterPlan router_plan(int T, int H, int E, bool shared_gate) {
+  RouterPlan p{};
+  const int ne_wr = (E + 15) / 16 * 16;
+  p.fused_gate = shared_gate && ne_wr + 16 <= 256;
+  p.NE = ne_wr + (p.fused_gate ? 16 : 0);
+  const int m_tiles = (T + kTileM - 1) / kTileM;
+  const int KB = H / kTileK;
+  // Enough K slices to put ~152 CTAs to work, at least 2 k-blocks each, and at
+  // most ~32 MB of partial logits.  Depends on the shapes only.
+  int ks = 152 / (m_tiles > 0 ? m_tiles : 1);
+  if (ks > KB / 2) ks = KB / 2;
+  const long long per_slice = static_cast<long long>(T) * p.NE * 4;
+  if (per_slice > 0 && ks * per_slice > (32ll << 20)) ks = static_cast<int>((32ll << 20) / per_slice);
+  if (ks < 1) ks = 1;
+  const int kbs = (KB + ks - 1) / ks;
+  p.ksplit = (KB + kbs - 1) / kbs;
+  p.kb_per_split = kbs;
+  p.scratch_bytes = static_cast<size_t>(p.ksplit) * per_slice;
+  return p;
+}
+
+cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_wr, const CUtensorMap* map_ws, int T,
+                          int H, int E, int k, const RouteSpec& spec, const void* x, const void* w_shared_gate,
+                          int32_t* topk_idx, float* topk_w, float* shared_scale, void* scratch, uint32_t* err,
+                          cudaStream_t stream) {
+  const RouterPlan p = router_plan(T, H, E, w_shared_gate != nullptr && shared_scale != nullptr);
+  GemmArgs g{};
+  g.T = T;
+  g.H = H;
+  g.NE = p.NE;
+  g.n_wr_boxes = (E + 15) / 16;
+  g.gate_box = p.fused_gate ? g.n_wr_boxes : -1;
+  g.tmem_cols = p.NE <= 32 ? 32 : p.NE <= 64 ? 64 : p.NE <= 128 ? 128 : 256;
+  g.kb_per_split = p.kb_per_split;
+  g.partial = static_cast<float*>(scratch);
+  g.err = err;
+  const int stage_bytes = kATileBytes + p.NE * kTileK * 2;
+  const int fixed = 1024 + (2 * kMaxStages + 2) * 8 + 64;
+  int stages = (227 * 1024 - fixed) / stage_bytes;
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages > p.kb_per_split) stages = p.kb_per_split;
+  g.stages = stages;
+  const size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(stages) * stage_bytes;
+
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(router_topk_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         227 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int grid = (a.T + kTileM - 1) / kTileM;
-  router_topk_kernel<KMAX><<<grid, kThreads, smem, stream>>>(mx, mw, a);
-  return cudaGetLastError();
-}
+  const dim3 grid((T + kTileM - 1) / kTileM, p.ksplit);
+  router_gemm_kernel<<<grid, kThreads, smem, stream>>>(map_x, map_wr, p.fused_gate ? *map_ws : map_wr, g);
 
-}  // namespace
-
-cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_wr, int T, int H, int E, int k,
-                          const RouteSpec& spec, int32_t* topk_idx, float* topk_w, uint32_t* err,
-                          cudaStream_t stream) {
-  RouterArgs a{};
-  a.T = T;
-  a.H = H;
-  a.E = E;
-  a.k = k;
-  a.NE = (E + 15) / 16 * 16;
-  a.tmem_cols = a.NE <= 32 ? 32 : a.NE <= 64 ? 64 : a.NE <= 128 ? 128 : 256;
-  a.spec = spec;
-  a.topk_idx = topk_idx;
-  a.topk_w = topk_w;
-  a.err = err;
-  const int stage_bytes = kATileBytes + a.NE * kTileK * 2;
-  const int fixed = 1024 + 256 * 4 + (2 * kMaxStages + 2) * 8 + 64;
-  int stages = (227 * 1024 - fixed) / stage_bytes;
-  const int KB = H / kTileK;
-  if (stages > kMaxStages) stages = kMaxStages;
-  if (stages > KB) stages = KB;
-  a.stages = stages;
-  const size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(stages) * stage_bytes;
-  if (k <= 2) return launch_router_k<2>(map_x, map_wr, a, smem, stream);
-  if (k <= 4) return launch_router_k<4>(map_x, map_wr, a, smem, stream);
-  if (k <= 8) return launch_router_k<8>(map_x, map_wr, a, smem, stream);
-  return launch_router_k<16>(map_x, map_wr, a, smem, stream);
-}
-
-cudaError_t launch_shared_gate(const void* x, const void* w_s, int T, int H, float* shared_scale,
-                               cudaStream_t stream) {
-  const int threads = 256;
-  const int grid = (T * 32 + threads - 1) / threads;
-  shared_gate_kernel<<<grid, threads, 0, stream>>>(static_cast<const __nv_bfloat16*>(x),
-                                                   static_cast<const __nv_bfloat16*>(w_s), T, H, shared_scale);
+  TopkArgs t{};
+  t.partial = g.partial;
+  t.ksplit = p.ksplit;
+  t.T = T;
+  t.NE = p.NE;
+  t.E = E;
+  t.k = k;
+  t.gate_col = p.fused_gate ? g.n_wr_boxes * 16 : -1;
+  t.spec = spec;
+  t.topk_idx = topk_idx;
+  t.topk_w = topk_w;
+  t.shared_scale = shared_scale;
+  const int warps = 8;
+  router_topk_kernel<<<(T + warps - 1) / warps, warps * 32, 0, stream>>>(t);
+  if (w_shared_gate != nullptr && shared_scale != nullptr && !p.fused_gate) {
+    shared_gate_kernel<<<(T * 32 + 255) / 256, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x),
+                                                                 static_cast<const __nv_bfloat16*>(w_shared_gate),
+                                                                 T, H, shared_scale);
+  }
   return cudaGetLastError();
 }
 

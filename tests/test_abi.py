@@ -67,12 +67,12 @@ def test_workspace_sizes(lib):
     (4, 512, 8, 17, 2),    # k > 16
 ])
 def test_route_rejects_bad_shapes_without_a_launch(lib, T, H, E, k, status):
-    assert lib.moe_route(None, None, None, T, H, E, k, None, None, None, None) == status
+    assert lib.moe_route(None, None, None, T, H, E, k, None, None, None, None, 0, None) == status
 
 
 def test_null_and_misaligned_pointers_rejected(lib):
-    assert lib.moe_route(None, None, None, 4, 512, 8, 2, None, None, None, None) == 1
-    assert lib.moe_route(None, 0x1008, 0x2000, 4, 512, 8, 2, 0x3000, 0x4000, None, None) == 1  # misaligned x
+    assert lib.moe_route(None, None, None, 4, 512, 8, 2, None, None, None, None, 0, None) == 1
+    assert lib.moe_route(None, 0x1008, 0x2000, 4, 512, 8, 2, 0x3000, 0x4000, None, 0x5000, 1 << 20, None) == 1  # misaligned x
     assert lib.moe_forward_ex(None, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 4, 512, 1024, 8, 2, 0x6000,
                               0x7000, 16, None) == 3  # workspace too small
     assert lib.moe_combine(None, None, None, None, None, 4, 512, 2, None, None) == 1
@@ -83,15 +83,16 @@ def test_bad_group_config_rejected(lib):
     c = moe.MoeConfig()
     lib.moe_config_default(ctypes.byref(c))
     c.n_group, c.topk_group, c.group_topn = 8, 9, 2  # keeps more groups than exist
-    assert lib.moe_route(ctypes.byref(c), 0x1000, 0x2000, 4, 512, 256, 8, 0x3000, 0x4000, None, None) == 1
+    assert lib.moe_route(ctypes.byref(c), 0x1000, 0x2000, 4, 512, 256, 8, 0x3000, 0x4000, None, 0x5000, 1 << 20, None) == 1
     c.n_group, c.topk_group, c.group_topn = 7, 4, 2  # 256 experts do not split into 7 groups
-    assert lib.moe_route(ctypes.byref(c), 0x1000, 0x2000, 4, 512, 256, 8, 0x3000, 0x4000, None, None) == 2
+    assert lib.moe_route(ctypes.byref(c), 0x1000, 0x2000, 4, 512, 256, 8, 0x3000, 0x4000, None, 0x5000, 1 << 20, None) == 2
     c.n_group, c.topk_group, c.group_topn = 8, 1, 2  # k=8 > one group of 4 experts
-    assert lib.moe_route(ctypes.byref(c), 0x1000, 0x2000, 4, 512, 32, 8, 0x3000, 0x4000, None, None) == 1
+    assert lib.moe_route(ctypes.byref(c), 0x1000, 0x2000, 4, 512, 32, 8, 0x3000, 0x4000, None, 0x5000, 1 << 20,
+                         None) == 1
 
 
 def test_zero_tokens_is_a_noop(lib):
-    assert lib.moe_route(None, 0x1000, 0x2000, 0, 512, 8, 2, 0x3000, 0x4000, None, None) == 0
+    assert lib.moe_route(None, 0x1000, 0x2000, 0, 512, 8, 2, 0x3000, 0x4000, None, None, 0, None) == 0
     assert lib.moe_forward_ex(None, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0, 512, 1024, 8, 2, 0x6000,
                               0x7000, 0, None) == 0
     assert lib.moe_combine(None, None, None, None, None, 0, 512, 2, None, None) == 0
@@ -112,3 +113,11 @@ def test_package_has_no_cpu_fallback():
 def test_selftest_limit_checked_on_host(lib):
     assert lib.moe_selftest_wait_timeout(0, None) == 1
     assert lib.moe_selftest_wait_timeout(2000000, None) == 1
+
+
+def test_route_scratch_checked_before_launch(lib):
+    need = lib.moe_route_scratch_bytes(None, 4, 512, 8)
+    assert need >= 4 * 16 * 4
+    assert lib.moe_route(None, 0x1000, 0x2000, 4, 512, 8, 2, 0x3000, 0x4000, None, 0x5000, need - 1, None) == 3
+    assert lib.moe_route(None, 0x1000, 0x2000, 4, 512, 8, 2, 0x3000, 0x4000, None, None, need, None) == 1
+    assert lib.moe_route_scratch_bytes(None, 4, 500, 8) == 0
