@@ -54,6 +54,7 @@ struct SegDev {
 struct GemmArgs {
   SegDev seg[2];
   int nseg;
+  int munit;  // weight rows per tile: 128, or 256 for a CTA pair
   int stages;
   int kps;  // 64-wide K blocks per pipeline stage (one 3-D TMA box each)
   int bn_max;
@@ -102,7 +103,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const Sched& sc, 
   const int tr = sc.trows[t.s][lo];
   t.mb = local / ntb;
   t.tb = local - t.mb * ntb;
-  t.a_row = lo * sg.nout + t.mb * kTileM;
+  t.a_row = lo * sg.nout + t.mb * a.munit;
   t.b_row = sc.rowstart[t.s][lo] + t.tb * tr;
   t.valid = min(tr, rows_g - t.tb * tr);
   const int KB = sg.K / (kTileK * a.kps);  // stages of kps K blocks
@@ -118,7 +119,7 @@ __device__ void build_schedule(const GemmArgs& a, Sched& sc) {
   int total = 0;
   for (int s = 0; s < a.nseg; ++s) {
     const SegDev& sg = a.seg[s];
-    const int mblocks = sg.nout / kTileM;
+    const int mblocks = sg.nout / a.munit;
     for (int base = 0; base < sg.groups; base += 32) {
       const int g = base + lane;
       int start = 0, rows_g = 0;
@@ -160,15 +161,21 @@ __device__ void build_schedule(const GemmArgs& a, Sched& sc) {
   if (lane == 0 && a.nseg == 1) sc.seg_end[1] = total;
 }
 
-template <int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
+// The kernel body.  PAIR: the two CTAs of a cluster work as one CTA pair
+// (tcgen05 cta_group::2): a tile covers 256 weight rows, CTA r holds weight
+// rows [128 r, 128 r + 128) and token rows [N/2 r, N/2 r + N/2) of it, the
+// even CTA issues the M=256 MMAs for both and every TMA load of the pair
+// completes on the even CTA's full barrier.  Each CTA receives its 128 rows
+// of D in its own TMEM and runs its own epilogue.
+template <int EPI, bool PAIR>
+__device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& a) {
   constexpr int NUM_A = (EPI == kEpiSwiGLU) ? 2 : 1;
+  constexpr int BDIV = PAIR ? 2 : 1;  // share of the token rows held by one CTA
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages;
   const int KPS = a.kps;
-  const int stage_bytes = KPS * (NUM_A * kATileBytes + a.bn_max * kTileK * 2);
+  const int stage_bytes = KPS * (NUM_A * kATileBytes + (a.bn_max / BDIV) * kTileK * 2);
   uint8_t* staging = smem + S * stage_bytes;
   Sched* sched = reinterpret_cast<Sched*>(staging + kStagingBytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(sched + 1);
@@ -178,6 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0;
+  const int first = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int stride = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (warp == 0) build_schedule(a, *sched);
   if (threadIdx.x == 64) {
@@ -187,17 +197,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);
+      mbar_init(&tempty[i], 4 * BDIV);  // every epilogue warp of the pair
     }
     fence_mbar_init();
   }
   if (warp == 1) {
     __syncwarp();
-    tmem_alloc(tmem_holder, a.tmem_cols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(tmem_holder, a.tmem_cols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_holder, a.tmem_cols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the peer's barriers exist before any remote use
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_holder;
   const Sched& sc = *sched;
@@ -207,8 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- TMA producer
     // One elected lane: wait for a free slot, post the byte count, issue the
     // loads of the weight tile(s) and of the token tile.  The token box is
-    // always bn rows (one request); rows past the tile's own are not used.
-    // Several smaller boxes per tile were measured to be much slower.
+    // always bn rows (bn/2 per CTA of a pair; one request); rows past the
+    // tile's own are not used.  Several smaller boxes per tile were measured
+    // to be much slower.
     int it = 0;
     if (lane == 0) {
       for (int sg = 0; sg < a.nseg; ++sg) {
@@ -217,10 +234,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&maps.seg[sg].b);
       }
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = first; tile < total && ok; tile += stride) {
         const Tile t = decode_tile(a, sc, tile);
         const SegMaps& m = maps.seg[t.s];
-        const uint32_t bytes = KPS * (NUM_A * kATileBytes + t.bn * kTileK * 2);
+        const int n_tile = MOE_EXACT_N ? ((t.valid + 15) >> 4) << 4 : t.bn;
+        const int a_row = t.a_row + static_cast<int>(rank) * kTileM;
+        const int b_row = t.b_row + static_cast<int>(rank) * (n_tile / BDIV);
+        const uint32_t bytes = BDIV * KPS * (NUM_A * kATileBytes + (t.bn / BDIV) * kTileK * 2);
         for (int kb = t.kb0; kb < t.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
@@ -228,31 +248,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], bytes);
           uint8_t* st = smem + s * stage_bytes;
           uint8_t* sb = st + KPS * NUM_A * kATileBytes;
-          if (KPS == 1) {  // 2-D maps
-            tma_load_2d(st, &m.a0, &full[s], kb * kTileK, t.a_row);
-            if (NUM_A == 2) tma_load_2d(st + kATileBytes, &m.a1, &full[s], kb * kTileK, t.a_row);
-            tma_load_2d(sb, &m.b, &full[s], kb * kTileK, t.b_row);
-          } else {  // 3-D maps: KPS consecutive K blocks per request
-            tma_load_3d(st, &m.a0, &full[s], 0, t.a_row, kb * KPS);
-            if (NUM_A == 2) tma_load_3d(st + KPS * kATileBytes, &m.a1, &full[s], 0, t.a_row, kb * KPS);
-            tma_load_3d(sb, &m.b, &full[s], 0, t.b_row, kb * KPS);
+          if (PAIR) {
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], bytes);
+            const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
+            if (KPS == 1) {
+              tma_load_2d_pair(st, &m.a0, bar, kb * kTileK, a_row);
+              if (NUM_A == 2) tma_load_2d_pair(st + kATileBytes, &m.a1, bar, kb * kTileK, a_row);
+              tma_load_2d_pair(sb, &m.b, bar, kb * kTileK, b_row);
+            } else {
+              tma_load_3d_pair(st, &m.a0, bar, 0, a_row, kb * KPS);
+              if (NUM_A == 2) tma_load_3d_pair(st + KPS * kATileBytes, &m.a1, bar, 0, a_row, kb * KPS);
+              tma_load_3d_pair(sb, &m.b, bar, 0, b_row, kb * KPS);
+            }
+          } else {
+            mbar_arrive_expect_tx(&full[s], bytes);
+            if (KPS == 1) {  // 2-D maps
+              tma_load_2d(st, &m.a0, &full[s], kb * kTileK, a_row);
+              if (NUM_A == 2) tma_load_2d(st + kATileBytes, &m.a1, &full[s], kb * kTileK, a_row);
+              tma_load_2d(sb, &m.b, &full[s], kb * kTileK, b_row);
+            } else {  // 3-D maps: KPS consecutive K blocks per request
+              tma_load_3d(st, &m.a0, &full[s], 0, a_row, kb * KPS);
+              if (NUM_A == 2) tma_load_3d(st + KPS * kATileBytes, &m.a1, &full[s], 0, a_row, kb * KPS);
+              tma_load_3d(sb, &m.b, &full[s], 0, b_row, kb * KPS);
+            }
           }
         }
       }
+      // Do not leave while copies into this CTA's shared memory are in flight:
+      // wait until the last stages were consumed (their loads had landed).
+      for (int i = (it > S ? it - S : 0); i < it; ++i) {
+        if (PAIR)
+          mbar_wait(&empty[i % S], (i / S) & 1, a.err, kSiteTeardown);
+        else
+          mbar_wait(&full[i % S], (i / S) & 1, a.err, kSiteTeardown);
+      }
     }
-    // Do not leave while copies into this CTA's shared memory are in flight.
-    if (lane == 0)
-      for (int i = (it > S ? it - S : 0); i < it; ++i) mbar_wait(&full[i % S], (i / S) & 1, a.err, kSiteTeardown);
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       int it = 0, n = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
+      for (int tile = first; tile < total && ok; tile += stride, ++n) {
         const Tile t = decode_tile(a, sc, tile);
         const int acc = n % a.acc_stages;
         const uint32_t aph = (n / a.acc_stages) & 1;
@@ -260,7 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t d0 = tmem_base + acc * a.acc_cols;
         const uint32_t d1 = d0 + a.bn_max;
-        const uint32_t idesc = idesc_bf16_f32(kTileM, MOE_EXACT_N ? ((t.valid + 15) >> 4) << 4 : t.bn);
+        const int n_tile = MOE_EXACT_N ? ((t.valid + 15) >> 4) << 4 : t.bn;
+        const uint32_t idesc = idesc_bf16_f32(kTileM * BDIV, n_tile);
         for (int kb = t.kb0; kb < t.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
@@ -271,28 +311,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after_sync();
           const uint32_t a0 = smem_u32(smem + s * stage_bytes);
           const uint32_t bb = a0 + KPS * NUM_A * kATileBytes;
-          const uint32_t b_atom = t.bn * kTileK * 2;
+          const uint32_t b_atom = (t.bn / BDIV) * kTileK * 2;
           for (int j = 0; j < KPS; ++j) {
 #pragma unroll
             for (int kk = 0; kk < kTileK / 16; ++kk) {
               const uint64_t bdesc = sdesc_k128(bb + j * b_atom + kk * 32);
               const uint32_t accum = (kb != t.kb0 || j != 0 || kk != 0);
-              umma_bf16(d0, sdesc_k128(a0 + j * kATileBytes + kk * 32), bdesc, idesc, accum);
-              if (NUM_A == 2)
-                umma_bf16(d1, sdesc_k128(a0 + (KPS + j) * kATileBytes + kk * 32), bdesc, idesc, accum);
+              const uint64_t adesc0 = sdesc_k128(a0 + j * kATileBytes + kk * 32);
+              if (PAIR) {
+                umma_bf16_pair(d0, adesc0, bdesc, idesc, accum);
+                if (NUM_A == 2)
+                  umma_bf16_pair(d1, sdesc_k128(a0 + (KPS + j) * kATileBytes + kk * 32), bdesc, idesc, accum);
+              } else {
+                umma_bf16(d0, adesc0, bdesc, idesc, accum);
+                if (NUM_A == 2)
+                  umma_bf16(d1, sdesc_k128(a0 + (KPS + j) * kATileBytes + kk * 32), bdesc, idesc, accum);
+              }
             }
           }
-          umma_commit(&empty[s]);
+          if (PAIR)
+            umma_commit_pair(&empty[s]);
+          else
+            umma_commit(&empty[s]);
         }
-        umma_commit(&tfull[acc]);
+        if (PAIR)
+          umma_commit_pair(&tfull[acc]);
+        else
+          umma_commit(&tfull[acc]);
       }
     }
   } else {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;
     uint8_t* stg = staging + (warp - 2) * (32 * 32 * 4);
+    const uint32_t tempty_leader = PAIR ? mapa_shared(smem_u32(&tempty[0]), 0) : 0;
     int n = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++n) {
+    for (int tile = first; tile < total; tile += stride, ++n) {
       const Tile t = decode_tile(a, sc, tile);
       const int acc = n % a.acc_stages;
       const uint32_t aph = (n / a.acc_stages) & 1;
@@ -300,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const SegDev& sg = a.seg[t.s];
       const uint32_t col0 = acc * a.acc_cols;
-      const int feat0 = t.mb * kTileM + q * 32;
+      const int feat0 = t.mb * a.munit + static_cast<int>(rank) * kTileM + q * 32;
       const int ncols = MOE_EXACT_N ? ((t.valid + 15) >> 4) << 4 : t.bn;  // the columns the MMA wrote
       for (int c0 = 0; c0 < ncols; c0 += 32) {
         const int nc = min(32, ncols - c0);
@@ -354,29 +408,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) {
+        if (PAIR)
+          mbar_arrive_cluster(tempty_leader + acc * 8);
+        else
+          mbar_arrive(&tempty[acc]);
+      }
     }
   }
 
   __syncthreads();
+  if (PAIR) cluster_sync();  // the pair is done with TMEM and with each other's barriers
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, a.tmem_cols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, a.tmem_cols);
+    else
+      tmem_dealloc(tmem_base, a.tmem_cols);
   }
 }
 
 template <int EPI>
-cudaError_t launch_epi(const GemmArgs& a, const GemmMaps& maps, int grid, size_t smem, cudaStream_t stream) {
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmMaps maps,
+                                                                    const GemmArgs a) {
+  gemm_body<EPI, false>(maps, a);
+}
+
+template <int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
+  gemm_body<EPI, true>(maps, a);
+}
+
+template <int EPI>
+cudaError_t launch_epi(const GemmArgs& a, const GemmMaps& maps, int grid, size_t smem, bool pair,
+                       cudaStream_t stream) {
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          227 * 1024);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               227 * 1024);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  grouped_gemm_kernel<EPI><<<grid, kThreads, smem, stream>>>(maps, a);
+  if (pair)
+    grouped_gemm_pair_kernel<EPI><<<grid, kThreads, smem, stream>>>(maps, a);
+  else
+    grouped_gemm_kernel<EPI><<<grid, kThreads, smem, stream>>>(maps, a);
   return cudaGetLastError();
 }
 
@@ -396,60 +478,74 @@ int bn_max_of(int num_segments, const GemmSegment* segs) {
 
 }  // namespace
 
-// Largest number of 64-wide K blocks per pipeline stage (1, 2, 4; at most
-// MOE_KPS_MAX) that divides every segment's K slices and still leaves three
-// stages in shared memory.  Longer stages fetch longer contiguous runs of
-// each weight row per TMA request.
+// CTA pairs (tcgen05 cta_group::2) halve the token rows each CTA stages and
+// reads, which is what limits the large-tile, tensor-bound GEMMs; they need
+// weight blocks of 256 rows.  Measured on GB300: with 256-row token tiles the
+// down projection runs 18-20 % faster as pairs (Mixtral T=4096, DeepSeek-V3
+// T=8192); with 128-row or smaller tiles pairs gain nothing or lose a little.
+#ifndef MOE_PAIR_MIN_BN
+#define MOE_PAIR_MIN_BN 256
+#endif
+// Measured on GB300 (Mixtral-, Qwen2- and DeepSeek-V3-shaped layers): the
+// SwiGLU GEMM gains from 2-block stages even with only two stages once its
+// token tiles are >= 64 rows; the fp32-store GEMM needs three stages.
 #ifndef MOE_KPS_MAX
 #define MOE_KPS_MAX 2
 #endif
-int grouped_gemm_kps(GemmEpilogue epi, int num_segments, const GemmSegment* segs) {
+GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment* segs) {
+  GemmPlan p{};
   const int num_a = (epi == kEpiSwiGLU) ? 2 : 1;
-  const int per_kb = num_a * kATileBytes + bn_max_of(num_segments, segs) * kTileK * 2;
-  int kps = 1;
+  const int bn_max = bn_max_of(num_segments, segs);
+  p.pair = MOE_PAIR_MIN_BN > 0 && bn_max >= MOE_PAIR_MIN_BN;
+  for (int s = 0; s < num_segments; ++s) p.pair = p.pair && segs[s].nout % (2 * kTileM) == 0;
+  const int per_kb = num_a * kATileBytes + (p.pair ? bn_max / 2 : bn_max) * kTileK * 2;
+  const int min_stages = (epi == kEpiSwiGLU && bn_max >= 64) ? 2 : 3;
+  p.kps = 1;
   for (int cand = 2; cand <= MOE_KPS_MAX; cand <<= 1) {
-    bool ok = (227 * 1024 - kFixedSmem) / (cand * per_kb) >= 3;
+    bool ok = (227 * 1024 - kFixedSmem) / (cand * per_kb) >= min_stages;
     for (int s = 0; s < num_segments && ok; ++s) {
       const int ks = (epi == kEpiSwiGLU || segs[s].ksplit < 1) ? 1 : segs[s].ksplit;
       ok = segs[s].K % (kTileK * cand) == 0 && segs[s].K / (kTileK * cand) >= 2 * ks;
     }
-    if (ok) kps = cand;
+    if (ok) p.kps = cand;
   }
-  return kps;
+  return p;
 }
 
 cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSegment* segs, const SegMaps* seg_maps,
                                 int num_sms, uint32_t* err, cudaStream_t stream) {
+  const GemmPlan plan = grouped_gemm_plan(epi, num_segments, segs);
   GemmArgs a{};
   a.nseg = num_segments;
   a.err = err;
+  a.munit = plan.pair ? 2 * kTileM : kTileM;
   long long upper = 0;
   for (int s = 0; s < num_segments; ++s) {
     const GemmSegment& g = segs[s];
     const int ks = (epi == kEpiSwiGLU || g.ksplit < 1) ? 1 : g.ksplit;
     a.seg[s] = SegDev{g.offsets, g.groups, g.rows, g.nout, g.K, g.bn, g.ldo, ks, g.slice_stride, g.out};
     a.bn_max = a.bn_max > g.bn ? a.bn_max : g.bn;
-    upper += static_cast<long long>(g.nout / kTileM) * ((g.rows + g.bn - 1) / g.bn + g.groups) * ks;
+    upper += static_cast<long long>(g.nout / a.munit) * ((g.rows + g.bn - 1) / g.bn + g.groups) * ks;
   }
   const int num_a = (epi == kEpiSwiGLU) ? 2 : 1;
   a.acc_cols = num_a * a.bn_max;
   a.acc_stages = (2 * a.acc_cols <= 512) ? 2 : 1;
   a.tmem_cols = static_cast<int>(pow2_at_least(static_cast<uint32_t>(a.acc_stages * a.acc_cols)));
-  a.kps = grouped_gemm_kps(epi, num_segments, segs);
-  const int stage_bytes = a.kps * (num_a * kATileBytes + a.bn_max * kTileK * 2);
-  const int fixed = kFixedSmem;
-  int stages = (227 * 1024 - fixed) / stage_bytes;
+  a.kps = plan.kps;
+  const int stage_bytes = a.kps * (num_a * kATileBytes + (plan.pair ? a.bn_max / 2 : a.bn_max) * kTileK * 2);
+  int stages = (227 * 1024 - kFixedSmem) / stage_bytes;
   if (stages > kMaxStages) stages = kMaxStages;
   a.stages = stages;
-  const size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(stages) * stage_bytes;
-  int grid = num_sms;
-  if (upper < grid) grid = static_cast<int>(upper);
-  if (grid < 1) grid = 1;
+  const size_t smem = static_cast<size_t>(kFixedSmem) + static_cast<size_t>(stages) * stage_bytes;
+  int units = plan.pair ? num_sms / 2 : num_sms;  // CTAs, or CTA pairs
+  if (upper < units) units = static_cast<int>(upper);
+  if (units < 1) units = 1;
+  const int grid = plan.pair ? 2 * units : units;
   GemmMaps maps;
   maps.seg[0] = seg_maps[0];
   maps.seg[1] = seg_maps[num_segments > 1 ? 1 : 0];
-  if (epi == kEpiSwiGLU) return launch_epi<kEpiSwiGLU>(a, maps, grid, smem, stream);
-  return launch_epi<kEpiStoreF32>(a, maps, grid, smem, stream);
+  if (epi == kEpiSwiGLU) return launch_epi<kEpiSwiGLU>(a, maps, grid, smem, plan.pair, stream);
+  return launch_epi<kEpiStoreF32>(a, maps, grid, smem, plan.pair, stream);
 }
 
 }  // namespace moe

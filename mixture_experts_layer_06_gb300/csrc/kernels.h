@@ -63,9 +63,16 @@ struct GemmSegment {
 
 enum GemmEpilogue { kEpiSwiGLU = 0, kEpiStoreF32 = 1 };
 
-// K blocks (of 64) per pipeline stage the grouped GEMM will use for these
-// segments; A maps and the full-tile B map must have that box depth.
-int grouped_gemm_kps(GemmEpilogue epi, int num_segments, const GemmSegment* segs);
+// How the grouped GEMM will run these segments: as CTA pairs (tcgen05
+// cta_group::2, 256-row weight tiles; each CTA stages bn/2 token rows) or
+// single CTAs, and with how many 64-wide K blocks per pipeline stage.  The A
+// maps and the token map must be built to match (token box bn/2 rows for a
+// pair; box depth kps).
+struct GemmPlan {
+  bool pair;
+  int kps;
+};
+GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment* segs);
 
 // TMA descriptors of one grouped-GEMM segment.  a0 / a1 cover the
 // [groups*nout, K] weights (gate and up for SwiGLU; a1 unused otherwise) with

@@ -158,11 +158,13 @@ moe::RouteSpec route_spec(const moe_config_t& c) {
   return s;
 }
 
-// Largest token tile of the SwiGLU GEMM.  Its two accumulators take 2*bn
-// TMEM columns, so bn <= 128 leaves room for two accumulator stages.
-#ifndef MOE_SWIGLU_BN_MAX
-#define MOE_SWIGLU_BN_MAX 256
-#endif
+// Token tile of the SwiGLU GEMM for a segment.  Its two accumulators take
+// 2*bn TMEM columns, so bn <= 128 leaves room for two accumulator stages
+// (the epilogue then overlaps the next tile's MMAs).  Measured on GB300: a
+// segment with >= 512 rows per group (Mixtral T=4096, a dense shared expert)
+// is faster with bn = 128; with ~256 rows per group (DeepSeek-V3 T=8192)
+// bn = 256 keeps the weight tile read once per group and wins.
+int swiglu_bn(long long rows, int groups);
 
 // Token tile of the grouped GEMM: the smallest of 16..bn_max that covers the
 // mean rows per group.
@@ -209,6 +211,16 @@ Split choose_split(const moe_config_t& c, int T, int H, int F, int E, int k) {
   }
   return sp;
 }
+
+int swiglu_bn(long long rows, int groups) {
+  const long long avg = (rows + groups - 1) / (groups > 0 ? groups : 1);
+  return choose_bn(rows, groups, avg >= 512 ? 128 : 256);
+}
+
+// Token tile of a dense shared-expert segment that shares a launch with the
+// routed segment: no larger than the routed tile (or 128), so that it does not
+// force bigger stages and fewer accumulator slots on the routed tiles.
+int shared_bn(long long rows, int routed_bn) { return choose_bn(rows, 1, routed_bn > 128 ? routed_bn : 128); }
 
 // Workspace carve-up of moe_forward_ex, 256-byte aligned pieces.
 struct Layout {
@@ -290,16 +302,17 @@ moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStre
   // gate+up: B = token rows [rows, H], A = gate / up weights [groups*F, H]
   for (int s = 0; s < nseg; ++s) {
     const FfnOperands& o = ops[s];
-    seg[s] = GemmSegment{o.offsets, o.groups, o.rows, o.F, o.H, choose_bn(o.rows, o.groups, MOE_SWIGLU_BN_MAX),
-                         o.h, o.F};
+    const int bn = (nseg > 1 && s == 1) ? shared_bn(o.rows, seg[0].bn) : swiglu_bn(o.rows, o.groups);
+    seg[s] = GemmSegment{o.offsets, o.groups, o.rows, o.F, o.H, bn, o.h, o.F};
   }
-  int kps = moe::grouped_gemm_kps(moe::kEpiSwiGLU, nseg, seg);
+  moe::GemmPlan plan = moe::grouped_gemm_plan(moe::kEpiSwiGLU, nseg, seg);
   for (int s = 0; s < nseg; ++s) {
     const FfnOperands& o = ops[s];
     const uint64_t wrows = static_cast<uint64_t>(o.groups) * o.F;
-    if (!make_gemm_map(&maps[s].a0, o.w_gate, wrows, o.H, 128, kps) ||
-        !make_gemm_map(&maps[s].a1, o.w_up, wrows, o.H, 128, kps) ||
-        !make_gemm_map(&maps[s].b, o.x_rows, o.rows, o.H, seg[s].bn, kps))
+    const uint32_t brows = plan.pair ? seg[s].bn / 2 : seg[s].bn;
+    if (!make_gemm_map(&maps[s].a0, o.w_gate, wrows, o.H, 128, plan.kps) ||
+        !make_gemm_map(&maps[s].a1, o.w_up, wrows, o.H, 128, plan.kps) ||
+        !make_gemm_map(&maps[s].b, o.x_rows, o.rows, o.H, brows, plan.kps))
       return MOE_ERR_CUDA;
   }
   if (moe::launch_grouped_gemm(moe::kEpiSwiGLU, nseg, seg, maps, d->num_sms, d->err, stream) != cudaSuccess)
@@ -307,15 +320,17 @@ moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStre
   // down: B = h [rows, F], A = down weights [groups*H, F]
   for (int s = 0; s < nseg; ++s) {
     const FfnOperands& o = ops[s];
-    seg[s] = GemmSegment{o.offsets, o.groups, o.rows, o.H, o.F, choose_bn(o.rows, o.groups), o.y, o.H, o.ksplit,
+    const int bn = (nseg > 1 && s == 1) ? shared_bn(o.rows, seg[0].bn) : choose_bn(o.rows, o.groups);
+    seg[s] = GemmSegment{o.offsets, o.groups, o.rows, o.H, o.F, bn, o.y, o.H, o.ksplit,
                          static_cast<size_t>(o.rows) * o.H};
   }
-  kps = moe::grouped_gemm_kps(moe::kEpiStoreF32, nseg, seg);
+  plan = moe::grouped_gemm_plan(moe::kEpiStoreF32, nseg, seg);
   for (int s = 0; s < nseg; ++s) {
     const FfnOperands& o = ops[s];
     const uint64_t wrows = static_cast<uint64_t>(o.groups) * o.H;
-    if (!make_gemm_map(&maps[s].a0, o.w_down, wrows, o.F, 128, kps) ||
-        !make_gemm_map(&maps[s].b, o.h, o.rows, o.F, seg[s].bn, kps))
+    const uint32_t brows = plan.pair ? seg[s].bn / 2 : seg[s].bn;
+    if (!make_gemm_map(&maps[s].a0, o.w_down, wrows, o.F, 128, plan.kps) ||
+        !make_gemm_map(&maps[s].b, o.h, o.rows, o.F, brows, plan.kps))
       return MOE_ERR_CUDA;
     maps[s].a1 = maps[s].a0;
   }
