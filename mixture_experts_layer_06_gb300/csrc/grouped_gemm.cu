@@ -43,6 +43,7 @@ constexpr int kTileK = 64;
 constexpr int kATileBytes = kTileM * kTileK * 2;  // 16 KB
 constexpr int kMaxSegGroups = 256;
 constexpr int kStagingBytes = 4 * 32 * 32 * 4;    // per-warp 32x32 fp32 transpose tiles
+constexpr int kXchgBytes = 4 * 2 * 32 * 32 * 4;    // split SwiGLU: per-warp double-buffered up chunks
 
 struct SegDev {
   const int32_t* offsets;
@@ -70,6 +71,12 @@ struct Sched {
   int trows[2][kMaxSegGroups];         // token rows per tile of each group
   int seg_end[2];                      // tile count after segment 0 / 1
 };
+
+// SiLU(g) = g / (1 + exp(-g)) with the fast divide; the input is clamped so
+// that the divisor stays finite (SiLU(-80) is 0 to far below bf16 resolution).
+__device__ __forceinline__ float silu(float g) {
+  return __fdividef(g, 1.f + __expf(-fmaxf(g, -80.f)));
+}
 
 struct GemmMaps {
   SegMaps seg[2];
@@ -169,6 +176,8 @@ __device__ void build_schedule(const GemmArgs& a, Sched& sc) {
 // of D in its own TMEM and runs its own epilogue.
 template <int EPI, bool PAIR>
 __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& a) {
+  constexpr bool SPLIT = (EPI == kEpiSwiGLUSplit);  // requires PAIR
+  static_assert(!SPLIT || PAIR, "split SwiGLU runs on CTA pairs");
   constexpr int NUM_A = (EPI == kEpiSwiGLU) ? 2 : 1;
   constexpr int BDIV = PAIR ? 2 : 1;  // share of the token rows held by one CTA
   extern __shared__ uint8_t smem_raw[];
@@ -177,12 +186,16 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
   const int KPS = a.kps;
   const int stage_bytes = KPS * (NUM_A * kATileBytes + (a.bn_max / BDIV) * kTileK * 2);
   uint8_t* staging = smem + S * stage_bytes;
-  Sched* sched = reinterpret_cast<Sched*>(staging + kStagingBytes);
+  // split SwiGLU: up values from the odd CTA land here, [warp][slot][lane][32]
+  float* xbuf = reinterpret_cast<float*>(staging + kStagingBytes);
+  Sched* sched = reinterpret_cast<Sched*>(staging + kStagingBytes + (SPLIT ? kXchgBytes : 0));
   uint64_t* full = reinterpret_cast<uint64_t*>(sched + 1);
   uint64_t* empty = full + kMaxStages;
   uint64_t* tfull = empty + kMaxStages;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* xfull = tempty + 2;   // [warp q][slot], even CTA: up values arrived
+  uint64_t* xempty = xfull + 8;   // [warp q][slot], odd CTA: slot consumed
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(xempty + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0;
@@ -198,6 +211,10 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 4 * BDIV);  // every epilogue warp of the pair
+    }
+    for (int i = 0; i < 8; ++i) {
+      mbar_init(&xfull[i], 1);
+      mbar_init(&xempty[i], 1);
     }
     fence_mbar_init();
   }
@@ -236,9 +253,11 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
       bool ok = true;
       for (int tile = first; tile < total && ok; tile += stride) {
         const Tile t = decode_tile(a, sc, tile);
-        const SegMaps& m = maps.seg[t.s];
+        const SegMaps& ms = maps.seg[t.s];
+        // split SwiGLU: the odd CTA loads the up rows into the A slot
+        const CUtensorMap* ma0 = (SPLIT && rank == 1) ? &ms.a1 : &ms.a0;
         const int n_tile = MOE_EXACT_N ? ((t.valid + 15) >> 4) << 4 : t.bn;
-        const int a_row = t.a_row + static_cast<int>(rank) * kTileM;
+        const int a_row = t.a_row + (SPLIT ? 0 : static_cast<int>(rank) * kTileM);
         const int b_row = t.b_row + static_cast<int>(rank) * (n_tile / BDIV);
         const uint32_t bytes = BDIV * KPS * (NUM_A * kATileBytes + (t.bn / BDIV) * kTileK * 2);
         for (int kb = t.kb0; kb < t.kb1; ++kb, ++it) {
@@ -254,24 +273,24 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
             if (rank == 0) mbar_arrive_expect_tx(&full[s], bytes);
             const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
             if (KPS == 1) {
-              tma_load_2d_pair(st, &m.a0, bar, kb * kTileK, a_row);
-              if (NUM_A == 2) tma_load_2d_pair(st + kATileBytes, &m.a1, bar, kb * kTileK, a_row);
-              tma_load_2d_pair(sb, &m.b, bar, kb * kTileK, b_row);
+              tma_load_2d_pair(st, ma0, bar, kb * kTileK, a_row);
+              if (NUM_A == 2) tma_load_2d_pair(st + kATileBytes, &ms.a1, bar, kb * kTileK, a_row);
+              tma_load_2d_pair(sb, &ms.b, bar, kb * kTileK, b_row);
             } else {
-              tma_load_3d_pair(st, &m.a0, bar, 0, a_row, kb * KPS);
-              if (NUM_A == 2) tma_load_3d_pair(st + KPS * kATileBytes, &m.a1, bar, 0, a_row, kb * KPS);
-              tma_load_3d_pair(sb, &m.b, bar, 0, b_row, kb * KPS);
+              tma_load_3d_pair(st, ma0, bar, 0, a_row, kb * KPS);
+              if (NUM_A == 2) tma_load_3d_pair(st + KPS * kATileBytes, &ms.a1, bar, 0, a_row, kb * KPS);
+              tma_load_3d_pair(sb, &ms.b, bar, 0, b_row, kb * KPS);
             }
           } else {
             mbar_arrive_expect_tx(&full[s], bytes);
             if (KPS == 1) {  // 2-D maps
-              tma_load_2d(st, &m.a0, &full[s], kb * kTileK, a_row);
-              if (NUM_A == 2) tma_load_2d(st + kATileBytes, &m.a1, &full[s], kb * kTileK, a_row);
-              tma_load_2d(sb, &m.b, &full[s], kb * kTileK, b_row);
+              tma_load_2d(st, ma0, &full[s], kb * kTileK, a_row);
+              if (NUM_A == 2) tma_load_2d(st + kATileBytes, &ms.a1, &full[s], kb * kTileK, a_row);
+              tma_load_2d(sb, &ms.b, &full[s], kb * kTileK, b_row);
             } else {  // 3-D maps: KPS consecutive K blocks per request
-              tma_load_3d(st, &m.a0, &full[s], 0, a_row, kb * KPS);
-              if (NUM_A == 2) tma_load_3d(st + KPS * kATileBytes, &m.a1, &full[s], 0, a_row, kb * KPS);
-              tma_load_3d(sb, &m.b, &full[s], 0, b_row, kb * KPS);
+              tma_load_3d(st, ma0, &full[s], 0, a_row, kb * KPS);
+              if (NUM_A == 2) tma_load_3d(st + KPS * kATileBytes, &ms.a1, &full[s], 0, a_row, kb * KPS);
+              tma_load_3d(sb, &ms.b, &full[s], 0, b_row, kb * KPS);
             }
           }
         }
@@ -345,6 +364,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
     const int q = warp & 3;
     uint8_t* stg = staging + (warp - 2) * (32 * 32 * 4);
     const uint32_t tempty_leader = PAIR ? mapa_shared(smem_u32(&tempty[0]), 0) : 0;
+    uint32_t cseq = 0;  // split SwiGLU: exchange chunk counter (same sequence in both CTAs)
     int n = 0;
     for (int tile = first; tile < total; tile += stride, ++n) {
       const Tile t = decode_tile(a, sc, tile);
@@ -354,8 +374,82 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
       tc_fence_after_sync();
       const SegDev& sg = a.seg[t.s];
       const uint32_t col0 = acc * a.acc_cols;
-      const int feat0 = t.mb * a.munit + static_cast<int>(rank) * kTileM + q * 32;
+      const int feat0 = t.mb * a.munit + (SPLIT ? 0 : static_cast<int>(rank) * kTileM) + q * 32;
       const int ncols = MOE_EXACT_N ? ((t.valid + 15) >> 4) << 4 : t.bn;  // the columns the MMA wrote
+      if constexpr (SPLIT) {
+        // Odd CTA: its TMEM holds the up projection of the pair's features;
+        // ship each 32-column chunk to the even CTA's exchange slot.  Even CTA:
+        // gate projection in TMEM, up arrives in the slot; finish
+        // SiLU(gate) * up and write h.  Slot rows are XOR-swizzled by lane.
+        bool ok = true;
+        for (int c0 = 0; c0 < ncols && ok; c0 += 32, ++cseq) {
+          const int nc = min(32, ncols - c0);
+          const int slot = cseq & 1;
+          const uint32_t xph = (cseq >> 1) & 1;
+          float* xrow = xbuf + ((q * 2 + slot) * 32 + lane) * 32;
+          uint32_t g[32];
+          const uint32_t ta = tmem_addr(tmem_base, q * 32, col0 + c0);
+          if (nc == 32)
+            tmem_ld32(ta, g);
+          else
+            tmem_ld16(ta, g);
+          tmem_wait(g);
+          if (rank == 1) {
+            if (!mbar_wait(&xempty[q * 2 + slot], xph ^ 1, a.err, kSiteGemmEpilogue)) {
+              ok = false;
+              break;
+            }
+            const uint32_t rrow = mapa_shared(smem_u32(xrow), 0);
+            const uint32_t rbar = mapa_shared(smem_u32(&xfull[q * 2 + slot]), 0);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              if (v < nc / 4) st_async_v4(rrow + ((v ^ (lane & 7)) << 4), g[4 * v], g[4 * v + 1], g[4 * v + 2], g[4 * v + 3], rbar);
+          } else {
+            if (lane == 0) mbar_arrive_expect_tx(&xfull[q * 2 + slot], nc * 32 * 4);
+            __syncwarp();
+            if (!mbar_wait(&xfull[q * 2 + slot], xph, a.err, kSiteGemmEpilogue)) {
+              ok = false;
+              break;
+            }
+            float u[32];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              if (v < nc / 4) {
+                const float4 f = *reinterpret_cast<const float4*>(xrow + 4 * (v ^ (lane & 7)));
+                u[4 * v] = f.x;
+                u[4 * v + 1] = f.y;
+                u[4 * v + 2] = f.z;
+                u[4 * v + 3] = f.w;
+              }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&xempty[q * 2 + slot]), 1));
+            __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stg);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (j < nc) {
+                const float gv = __uint_as_float(g[j]);
+                st[j * 32 + lane] = __float2bfloat16_rn(silu(gv) * u[j]);
+              }
+            }
+            __syncwarp();
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
+            for (int v = lane; v < nc * 4; v += 32) {
+              const int j = v >> 2, piece = v & 3;
+              const int row = t.b_row + c0 + j;
+              if (c0 + j < t.valid && row < sg.rows)
+                *reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * sg.ldo + feat0 + piece * 8) =
+                    *reinterpret_cast<const uint4*>(st + j * 32 + piece * 8);
+            }
+            __syncwarp();
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_leader + acc * 8);
+        if (!ok) break;
+        continue;
+      }
       for (int c0 = 0; c0 < ncols; c0 += 32) {
         const int nc = min(32, ncols - c0);
         uint32_t g[32], u[32];
@@ -377,7 +471,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
           for (int j = 0; j < 32; ++j) {
             if (j < nc) {
               const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
-              st[j * 32 + lane] = __float2bfloat16_rn(gv / (1.f + __expf(-gv)) * uv);
+              st[j * 32 + lane] = __float2bfloat16_rn(silu(gv) * uv);
             }
           }
           __syncwarp();
@@ -440,25 +534,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   gemm_body<EPI, true>(maps, a);
 }
 
+template <typename K>
+cudaError_t allow_big_smem(K kernel, bool* configured) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || configured[dev]) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e == cudaSuccess) configured[dev] = true;
+  return e;
+}
+
 template <int EPI>
 cudaError_t launch_epi(const GemmArgs& a, const GemmMaps& maps, int grid, size_t smem, bool pair,
                        cudaStream_t stream) {
-  static bool configured[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         227 * 1024);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               227 * 1024);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
-  if (pair)
+  static bool single_ok[64] = {}, pair_ok[64] = {};
+  cudaError_t e;
+  if (pair) {
+    if ((e = allow_big_smem(grouped_gemm_pair_kernel<EPI>, pair_ok)) != cudaSuccess) return e;
     grouped_gemm_pair_kernel<EPI><<<grid, kThreads, smem, stream>>>(maps, a);
-  else
+  } else {
+    if ((e = allow_big_smem(grouped_gemm_kernel<EPI>, single_ok)) != cudaSuccess) return e;
     grouped_gemm_kernel<EPI><<<grid, kThreads, smem, stream>>>(maps, a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split(const GemmArgs& a, const GemmMaps& maps, int grid, size_t smem, cudaStream_t stream) {
+  static bool ok[64] = {};
+  cudaError_t e;
+  if ((e = allow_big_smem(grouped_gemm_pair_kernel<kEpiSwiGLUSplit>, ok)) != cudaSuccess) return e;
+  grouped_gemm_pair_kernel<kEpiSwiGLUSplit><<<grid, kThreads, smem, stream>>>(maps, a);
   return cudaGetLastError();
 }
 
@@ -468,7 +573,7 @@ uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
-constexpr int kFixedSmem = 1024 + kStagingBytes + static_cast<int>(sizeof(Sched)) + (2 * kMaxStages + 4) * 8 + 64;
+constexpr int kFixedSmem = 1024 + kStagingBytes + static_cast<int>(sizeof(Sched)) + (2 * kMaxStages + 4 + 16) * 8 + 64;
 
 int bn_max_of(int num_segments, const GemmSegment* segs) {
   int m = 16;
@@ -486,23 +591,38 @@ int bn_max_of(int num_segments, const GemmSegment* segs) {
 #ifndef MOE_PAIR_MIN_BN
 #define MOE_PAIR_MIN_BN 256
 #endif
+// The SwiGLU GEMM runs as split pairs (gate rows in the even CTA, up rows in
+// the odd one) when the token tiles of every segment reach this many rows
+// (0 = never).  Measured on GB300 it is slower than single CTAs (Mixtral
+// T=4096 gate+up 1600 vs 1467 us, DeepSeek-V3 T=8192 4423 vs 3794 us): the
+// per-chunk exchange through distributed shared memory costs more than the
+// operand traffic it saves.  Off by default.
+#ifndef MOE_SPLIT_MIN_BN
+#define MOE_SPLIT_MIN_BN 0
+#endif
 // Measured on GB300 (Mixtral-, Qwen2- and DeepSeek-V3-shaped layers): the
 // SwiGLU GEMM gains from 2-block stages even with only two stages once its
 // token tiles are >= 64 rows; the fp32-store GEMM needs three stages.
 #ifndef MOE_KPS_MAX
 #define MOE_KPS_MAX 2
 #endif
+
 GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment* segs) {
   GemmPlan p{};
-  const int num_a = (epi == kEpiSwiGLU) ? 2 : 1;
   const int bn_max = bn_max_of(num_segments, segs);
-  p.pair = MOE_PAIR_MIN_BN > 0 && bn_max >= MOE_PAIR_MIN_BN;
-  for (int s = 0; s < num_segments; ++s) p.pair = p.pair && segs[s].nout % (2 * kTileM) == 0;
+  int bn_min = bn_max;
+  for (int s = 0; s < num_segments; ++s) bn_min = bn_min < segs[s].bn ? bn_min : segs[s].bn;
+  p.split = epi == kEpiSwiGLU && MOE_SPLIT_MIN_BN > 0 && bn_min >= MOE_SPLIT_MIN_BN;
+  p.pair = p.split || (MOE_PAIR_MIN_BN > 0 && bn_max >= MOE_PAIR_MIN_BN);
+  if (!p.split)
+    for (int s = 0; s < num_segments; ++s) p.pair = p.pair && segs[s].nout % (2 * kTileM) == 0;
+  const int num_a = (epi == kEpiSwiGLU && !p.split) ? 2 : 1;
   const int per_kb = num_a * kATileBytes + (p.pair ? bn_max / 2 : bn_max) * kTileK * 2;
+  const int fixed = kFixedSmem + (p.split ? kXchgBytes : 0);
   const int min_stages = (epi == kEpiSwiGLU && bn_max >= 64) ? 2 : 3;
   p.kps = 1;
   for (int cand = 2; cand <= MOE_KPS_MAX; cand <<= 1) {
-    bool ok = (227 * 1024 - kFixedSmem) / (cand * per_kb) >= min_stages;
+    bool ok = (227 * 1024 - fixed) / (cand * per_kb) >= min_stages;
     for (int s = 0; s < num_segments && ok; ++s) {
       const int ks = (epi == kEpiSwiGLU || segs[s].ksplit < 1) ? 1 : segs[s].ksplit;
       ok = segs[s].K % (kTileK * cand) == 0 && segs[s].K / (kTileK * cand) >= 2 * ks;
@@ -518,7 +638,7 @@ cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSe
   GemmArgs a{};
   a.nseg = num_segments;
   a.err = err;
-  a.munit = plan.pair ? 2 * kTileM : kTileM;
+  a.munit = (plan.pair && !plan.split) ? 2 * kTileM : kTileM;
   long long upper = 0;
   for (int s = 0; s < num_segments; ++s) {
     const GemmSegment& g = segs[s];
@@ -527,16 +647,17 @@ cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSe
     a.bn_max = a.bn_max > g.bn ? a.bn_max : g.bn;
     upper += static_cast<long long>(g.nout / a.munit) * ((g.rows + g.bn - 1) / g.bn + g.groups) * ks;
   }
-  const int num_a = (epi == kEpiSwiGLU) ? 2 : 1;
+  const int num_a = (epi == kEpiSwiGLU && !plan.split) ? 2 : 1;
   a.acc_cols = num_a * a.bn_max;
   a.acc_stages = (2 * a.acc_cols <= 512) ? 2 : 1;
   a.tmem_cols = static_cast<int>(pow2_at_least(static_cast<uint32_t>(a.acc_stages * a.acc_cols)));
   a.kps = plan.kps;
   const int stage_bytes = a.kps * (num_a * kATileBytes + (plan.pair ? a.bn_max / 2 : a.bn_max) * kTileK * 2);
-  int stages = (227 * 1024 - kFixedSmem) / stage_bytes;
+  const int fixed = kFixedSmem + (plan.split ? kXchgBytes : 0);
+  int stages = (227 * 1024 - fixed) / stage_bytes;
   if (stages > kMaxStages) stages = kMaxStages;
   a.stages = stages;
-  const size_t smem = static_cast<size_t>(kFixedSmem) + static_cast<size_t>(stages) * stage_bytes;
+  const size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(stages) * stage_bytes;
   int units = plan.pair ? num_sms / 2 : num_sms;  // CTAs, or CTA pairs
   if (upper < units) units = static_cast<int>(upper);
   if (units < 1) units = 1;
@@ -544,6 +665,7 @@ cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSe
   GemmMaps maps;
   maps.seg[0] = seg_maps[0];
   maps.seg[1] = seg_maps[num_segments > 1 ? 1 : 0];
+  if (plan.split) return launch_split(a, maps, grid, smem, stream);
   if (epi == kEpiSwiGLU) return launch_epi<kEpiSwiGLU>(a, maps, grid, smem, plan.pair, stream);
   return launch_epi<kEpiStoreF32>(a, maps, grid, smem, plan.pair, stream);
 }

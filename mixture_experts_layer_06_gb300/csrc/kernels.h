@@ -61,7 +61,12 @@ struct GemmSegment {
   size_t slice_stride = 0; // elements
 };
 
-enum GemmEpilogue { kEpiSwiGLU = 0, kEpiStoreF32 = 1 };
+// kEpiSwiGLU: two accumulators (gate, up) per CTA.  kEpiSwiGLUSplit: CTA
+// pairs only; the pair's M=256 MMA puts 128 gate rows in the even CTA and the
+// matching 128 up rows in the odd CTA, which streams its up values to the
+// even CTA through distributed shared memory.  kEpiStoreF32: one accumulator,
+// fp32 out.
+enum GemmEpilogue { kEpiSwiGLU = 0, kEpiStoreF32 = 1, kEpiSwiGLUSplit = 2 };
 
 // How the grouped GEMM will run these segments: as CTA pairs (tcgen05
 // cta_group::2, 256-row weight tiles; each CTA stages bn/2 token rows) or
@@ -70,6 +75,7 @@ enum GemmEpilogue { kEpiSwiGLU = 0, kEpiStoreF32 = 1 };
 // pair; box depth kps).
 struct GemmPlan {
   bool pair;
+  bool split;  // SwiGLU as split pairs (kEpiSwiGLUSplit); implies pair
   int kps;
 };
 GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment* segs);
