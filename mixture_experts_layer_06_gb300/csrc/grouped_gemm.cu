@@ -14,16 +14,21 @@
 // Orientation: weights are the MMA's A operand (M = 128 weight rows of one
 // expert), tokens are B (N = bn tokens, 16..256), so a tile with few tokens
 // still runs a full-height MMA and streams weights at full width.  D^T tiles
-// live in TMEM: lane = output feature, column = token.
-//   SwiGLU:  two accumulators (gate rows, up rows) share every B tile;
-//            epilogue h = SiLU(g) * u -> bf16.
-//   Store:   one accumulator (down projection) -> fp32.
+// live in TMEM: lane = weight row, column = token.
+//   SwiGLU:  the 128-row A tile stacks 64 gate rows over the 64 up rows of
+//            the same features (one TMA box over a view in which gate and up
+//            are two planes), so ONE accumulator of bn columns holds both
+//            projections of a tile and two accumulator slots fit in TMEM:
+//            the epilogue of one tile overlaps the MMAs of the next.  The
+//            epilogue warps that read the gate lanes and the up lanes of the
+//            same features trade half of each 32-column chunk through shared
+//            memory and each finishes h = SiLU(g) * u for its half -> bf16.
+//   Store:   128 output rows per CTA (down projection) -> fp32.
 // Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
 // owner, warps 2-5 epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
 // Pipelines: a ring of `stages` shared-memory slots (full/empty mbarriers) and
-// one or two TMEM accumulator slots (tmem_full/tmem_empty mbarriers).  Every
-// wait is bounded; a wait that gives up records a device error and its role
-// stops.
+// two TMEM accumulator slots (tmem_full/tmem_empty mbarriers).  Every wait is
+// bounded; a wait that gives up records a device error and its role stops.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -42,12 +47,26 @@ constexpr int kTileM = 128;
 constexpr int kTileK = 64;
 constexpr int kATileBytes = kTileM * kTileK * 2;  // 16 KB
 constexpr int kMaxSegGroups = 256;
-constexpr int kStagingBytes = 4 * 32 * 32 * 4;    // per-warp 32x32 fp32 transpose tiles
-constexpr int kXchgBytes = 4 * 2 * 32 * 32 * 4;    // split SwiGLU: per-warp double-buffered up chunks
+constexpr int kHalfRows = 64;                    // SwiGLU: gate rows (= up rows) per A tile
+constexpr int kHalfBytes = kHalfRows * kTileK * 2;  // 8 KB
+// Epilogue shared memory.  Store: per-warp 32x32 fp32 transpose tiles.
+// SwiGLU: the exchange slots [warp pair][slot][half][lane][16 fp32] and
+// per-warp 16x32 bf16 output tiles.
+constexpr int kStoreStagingBytes = 4 * 32 * 32 * 4;
+constexpr int kXchgBytes = 2 * 2 * 2 * 32 * 16 * 4;
+constexpr int kSwiGLUStagingBytes = kXchgBytes + 4 * 16 * 32 * 2;
+__host__ __device__ constexpr int staging_bytes(int epi) {
+  return epi == kEpiSwiGLU ? kSwiGLUStagingBytes : kStoreStagingBytes;
+}
+// Output rows (features) per CTA and tile: 64 for SwiGLU (the A tile holds
+// their gate and up rows), 128 for the plain store.
+__host__ __device__ constexpr int feat_per_cta(int epi) { return epi == kEpiSwiGLU ? kHalfRows : kTileM; }
 
 struct SegDev {
   const int32_t* offsets;
   int groups, rows, nout, K, bn, ldo, ksplit;
+  int a_mode;    // SwiGLU A loads: kStackedMap or kTwoMaps
+  int up_first;  // stacked map: plane 0 is the up weights (lanes 0-63 = up)
   size_t slice_stride;
   void* out;
 };
@@ -55,12 +74,11 @@ struct SegDev {
 struct GemmArgs {
   SegDev seg[2];
   int nseg;
-  int munit;  // weight rows per tile: 128, or 256 for a CTA pair
+  int munit;  // output features per tile: NSUB * feat_per_cta(epi), x2 for a CTA pair
   int stages;
   int kps;  // 64-wide K blocks per pipeline stage (one 3-D TMA box each)
   int bn_max;
-  int acc_stages;
-  int acc_cols;
+  int acc_cols;  // TMEM columns per accumulator slot (two slots): NSUB * bn_max
   int tmem_cols;
   uint32_t* err;
 };
@@ -169,33 +187,29 @@ __device__ void build_schedule(const GemmArgs& a, Sched& sc) {
 }
 
 // The kernel body.  PAIR: the two CTAs of a cluster work as one CTA pair
-// (tcgen05 cta_group::2): a tile covers 256 weight rows, CTA r holds weight
-// rows [128 r, 128 r + 128) and token rows [N/2 r, N/2 r + N/2) of it, the
-// even CTA issues the M=256 MMAs for both and every TMA load of the pair
-// completes on the even CTA's full barrier.  Each CTA receives its 128 rows
-// of D in its own TMEM and runs its own epilogue.
-template <int EPI, bool PAIR>
+// (tcgen05 cta_group::2): a tile covers 2 x feat_per_cta(EPI) output features,
+// CTA r holds the A rows of its half of them and token rows
+// [N/2 r, N/2 r + N/2) of B, the even CTA issues the M=256 MMAs for both and
+// every TMA load of the pair completes on the even CTA's full barrier.  Each
+// CTA receives its 128 rows of D in its own TMEM and runs its own epilogue.
+template <int EPI, bool PAIR, int NSUB>
 __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& a) {
-  constexpr bool SPLIT = (EPI == kEpiSwiGLUSplit);  // requires PAIR
-  static_assert(!SPLIT || PAIR, "split SwiGLU runs on CTA pairs");
-  constexpr int NUM_A = (EPI == kEpiSwiGLU) ? 2 : 1;
+  constexpr bool SWIGLU = (EPI == kEpiSwiGLU);
   constexpr int BDIV = PAIR ? 2 : 1;  // share of the token rows held by one CTA
+  constexpr int FEAT = feat_per_cta(EPI);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages;
   const int KPS = a.kps;
-  const int stage_bytes = KPS * (NUM_A * kATileBytes + (a.bn_max / BDIV) * kTileK * 2);
+  const int stage_bytes = KPS * (NSUB * kATileBytes + (a.bn_max / BDIV) * kTileK * 2);
   uint8_t* staging = smem + S * stage_bytes;
-  // split SwiGLU: up values from the odd CTA land here, [warp][slot][lane][32]
-  float* xbuf = reinterpret_cast<float*>(staging + kStagingBytes);
-  Sched* sched = reinterpret_cast<Sched*>(staging + kStagingBytes + (SPLIT ? kXchgBytes : 0));
+  Sched* sched = reinterpret_cast<Sched*>(staging + staging_bytes(EPI));
   uint64_t* full = reinterpret_cast<uint64_t*>(sched + 1);
   uint64_t* empty = full + kMaxStages;
   uint64_t* tfull = empty + kMaxStages;
   uint64_t* tempty = tfull + 2;
-  uint64_t* xfull = tempty + 2;   // [warp q][slot], even CTA: up values arrived
-  uint64_t* xempty = xfull + 8;   // [warp q][slot], odd CTA: slot consumed
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(xempty + 8);
+  uint64_t* xfull = tempty + 2;  // SwiGLU: [warp pair][slot], both warps' values written
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(xfull + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0;
@@ -212,10 +226,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 4 * BDIV);  // every epilogue warp of the pair
     }
-    for (int i = 0; i < 8; ++i) {
-      mbar_init(&xfull[i], 1);
-      mbar_init(&xempty[i], 1);
-    }
+    for (int i = 0; i < 4; ++i) mbar_init(&xfull[i], 64);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -239,7 +250,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     // One elected lane: wait for a free slot, post the byte count, issue the
-    // loads of the weight tile(s) and of the token tile.  The token box is
+    // loads of the weight tile and of the token tile.  The token box is
     // always bn rows (bn/2 per CTA of a pair; one request); rows past the
     // tile's own are not used.  Several smaller boxes per tile were measured
     // to be much slower.
@@ -247,19 +258,18 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
     if (lane == 0) {
       for (int sg = 0; sg < a.nseg; ++sg) {
         tma_prefetch_map(&maps.seg[sg].a0);
-        if (NUM_A == 2) tma_prefetch_map(&maps.seg[sg].a1);
+        if (SWIGLU && a.seg[sg].a_mode == kTwoMaps) tma_prefetch_map(&maps.seg[sg].a1);
         tma_prefetch_map(&maps.seg[sg].b);
       }
       bool ok = true;
       for (int tile = first; tile < total && ok; tile += stride) {
         const Tile t = decode_tile(a, sc, tile);
         const SegMaps& ms = maps.seg[t.s];
-        // split SwiGLU: the odd CTA loads the up rows into the A slot
-        const CUtensorMap* ma0 = (SPLIT && rank == 1) ? &ms.a1 : &ms.a0;
+        const bool two_maps = SWIGLU && a.seg[t.s].a_mode == kTwoMaps;  // then KPS == 1
         const int n_tile = MOE_EXACT_N ? ((t.valid + 15) >> 4) << 4 : t.bn;
-        const int a_row = t.a_row + (SPLIT ? 0 : static_cast<int>(rank) * kTileM);
+        const int a_row = t.a_row + static_cast<int>(rank) * FEAT * NSUB;
         const int b_row = t.b_row + static_cast<int>(rank) * (n_tile / BDIV);
-        const uint32_t bytes = BDIV * KPS * (NUM_A * kATileBytes + (t.bn / BDIV) * kTileK * 2);
+        const uint32_t bytes = BDIV * KPS * (NSUB * kATileBytes + (t.bn / BDIV) * kTileK * 2);
         for (int kb = t.kb0; kb < t.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
@@ -268,30 +278,58 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
             break;
           }
           uint8_t* st = smem + s * stage_bytes;
-          uint8_t* sb = st + KPS * NUM_A * kATileBytes;
+          uint8_t* sb = st + KPS * NSUB * kATileBytes;
           if (PAIR) {
             if (rank == 0) mbar_arrive_expect_tx(&full[s], bytes);
             const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
-            if (KPS == 1) {
-              tma_load_2d_pair(st, ma0, bar, kb * kTileK, a_row);
-              if (NUM_A == 2) tma_load_2d_pair(st + kATileBytes, &ms.a1, bar, kb * kTileK, a_row);
-              tma_load_2d_pair(sb, &ms.b, bar, kb * kTileK, b_row);
+            if (two_maps) {
+              for (int u = 0; u < NSUB; ++u) {
+                tma_load_2d_pair(st + u * kATileBytes, &ms.a0, bar, kb * kTileK, a_row + u * kHalfRows);
+                tma_load_2d_pair(st + u * kATileBytes + kHalfBytes, &ms.a1, bar, kb * kTileK, a_row + u * kHalfRows);
+              }
+            } else if (SWIGLU) {
+              for (int u = 0; u < NSUB; ++u) {  // sub-tile u: its KPS A tiles, KPS * 16 KB
+                uint8_t* dst = st + u * KPS * kATileBytes;
+                if (KPS == 1)
+                  tma_load_3d_pair(dst, &ms.a0, bar, kb * kTileK, a_row + u * kHalfRows, 0);
+                else
+                  tma_load_4d_pair(dst, &ms.a0, bar, 0, a_row + u * kHalfRows, 0, kb * KPS);
+              }
             } else {
-              tma_load_3d_pair(st, ma0, bar, 0, a_row, kb * KPS);
-              if (NUM_A == 2) tma_load_3d_pair(st + KPS * kATileBytes, &ms.a1, bar, 0, a_row, kb * KPS);
-              tma_load_3d_pair(sb, &ms.b, bar, 0, b_row, kb * KPS);
+              if (KPS == 1)
+                tma_load_2d_pair(st, &ms.a0, bar, kb * kTileK, a_row);
+              else
+                tma_load_3d_pair(st, &ms.a0, bar, 0, a_row, kb * KPS);
             }
+            if (KPS == 1)
+              tma_load_2d_pair(sb, &ms.b, bar, kb * kTileK, b_row);
+            else
+              tma_load_3d_pair(sb, &ms.b, bar, 0, b_row, kb * KPS);
           } else {
             mbar_arrive_expect_tx(&full[s], bytes);
-            if (KPS == 1) {  // 2-D maps
-              tma_load_2d(st, ma0, &full[s], kb * kTileK, a_row);
-              if (NUM_A == 2) tma_load_2d(st + kATileBytes, &ms.a1, &full[s], kb * kTileK, a_row);
-              tma_load_2d(sb, &ms.b, &full[s], kb * kTileK, b_row);
-            } else {  // 3-D maps: KPS consecutive K blocks per request
-              tma_load_3d(st, ma0, &full[s], 0, a_row, kb * KPS);
-              if (NUM_A == 2) tma_load_3d(st + KPS * kATileBytes, &ms.a1, &full[s], 0, a_row, kb * KPS);
-              tma_load_3d(sb, &ms.b, &full[s], 0, b_row, kb * KPS);
+            if (two_maps) {
+              for (int u = 0; u < NSUB; ++u) {
+                tma_load_2d(st + u * kATileBytes, &ms.a0, &full[s], kb * kTileK, a_row + u * kHalfRows);
+                tma_load_2d(st + u * kATileBytes + kHalfBytes, &ms.a1, &full[s], kb * kTileK, a_row + u * kHalfRows);
+              }
+            } else if (SWIGLU) {
+              for (int u = 0; u < NSUB; ++u) {
+                uint8_t* dst = st + u * KPS * kATileBytes;
+                if (KPS == 1)
+                  tma_load_3d(dst, &ms.a0, &full[s], kb * kTileK, a_row + u * kHalfRows, 0);
+                else
+                  tma_load_4d(dst, &ms.a0, &full[s], 0, a_row + u * kHalfRows, 0, kb * KPS);
+              }
+            } else {
+              if (KPS == 1)
+                tma_load_2d(st, &ms.a0, &full[s], kb * kTileK, a_row);
+              else
+                tma_load_3d(st, &ms.a0, &full[s], 0, a_row, kb * KPS);
             }
+            if (KPS == 1)
+              tma_load_2d(sb, &ms.b, &full[s], kb * kTileK, b_row);
+            else
+              tma_load_3d(sb, &ms.b, &full[s], 0, b_row, kb * KPS);
           }
         }
       }
@@ -312,12 +350,11 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
       bool ok = true;
       for (int tile = first; tile < total && ok; tile += stride, ++n) {
         const Tile t = decode_tile(a, sc, tile);
-        const int acc = n % a.acc_stages;
-        const uint32_t aph = (n / a.acc_stages) & 1;
+        const int acc = n & 1;
+        const uint32_t aph = (n >> 1) & 1;
         if (!mbar_wait(&tempty[acc], aph ^ 1, a.err, kSiteGemmMma)) break;
         tc_fence_after_sync();
-        const uint32_t d0 = tmem_base + acc * a.acc_cols;
-        const uint32_t d1 = d0 + a.bn_max;
+        const uint32_t d = tmem_base + acc * a.acc_cols;
         const int n_tile = MOE_EXACT_N ? ((t.valid + 15) >> 4) << 4 : t.bn;
         const uint32_t idesc = idesc_bf16_f32(kTileM * BDIV, n_tile);
         for (int kb = t.kb0; kb < t.kb1; ++kb, ++it) {
@@ -329,22 +366,19 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
           }
           tc_fence_after_sync();
           const uint32_t a0 = smem_u32(smem + s * stage_bytes);
-          const uint32_t bb = a0 + KPS * NUM_A * kATileBytes;
+          const uint32_t bb = a0 + KPS * NSUB * kATileBytes;
           const uint32_t b_atom = (t.bn / BDIV) * kTileK * 2;
           for (int j = 0; j < KPS; ++j) {
 #pragma unroll
             for (int kk = 0; kk < kTileK / 16; ++kk) {
               const uint64_t bdesc = sdesc_k128(bb + j * b_atom + kk * 32);
               const uint32_t accum = (kb != t.kb0 || j != 0 || kk != 0);
-              const uint64_t adesc0 = sdesc_k128(a0 + j * kATileBytes + kk * 32);
-              if (PAIR) {
-                umma_bf16_pair(d0, adesc0, bdesc, idesc, accum);
-                if (NUM_A == 2)
-                  umma_bf16_pair(d1, sdesc_k128(a0 + (KPS + j) * kATileBytes + kk * 32), bdesc, idesc, accum);
-              } else {
-                umma_bf16(d0, adesc0, bdesc, idesc, accum);
-                if (NUM_A == 2)
-                  umma_bf16(d1, sdesc_k128(a0 + (KPS + j) * kATileBytes + kk * 32), bdesc, idesc, accum);
+              for (int u = 0; u < NSUB; ++u) {  // sub-tile u: A tile u*KPS+j, accumulator at column u*bn_max
+                const uint64_t adesc = sdesc_k128(a0 + (u * KPS + j) * kATileBytes + kk * 32);
+                if (PAIR)
+                  umma_bf16_pair(d + u * a.bn_max, adesc, bdesc, idesc, accum);
+                else
+                  umma_bf16(d + u * a.bn_max, adesc, bdesc, idesc, accum);
               }
             }
           }
@@ -362,31 +396,97 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
   } else {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;
-    uint8_t* stg = staging + (warp - 2) * (32 * 32 * 4);
     const uint32_t tempty_leader = PAIR ? mapa_shared(smem_u32(&tempty[0]), 0) : 0;
-    uint32_t cseq = 0;  // split SwiGLU: exchange chunk counter (same sequence in both CTAs)
+    // SwiGLU: warps q and q^2 read the gate and the up lanes of the same 32
+    // features (lanes 32q.. and 32(q^2)..); the low-lane warp finishes token
+    // columns [0,16) of every 32-column chunk, the other [16,32).
+    const int half = q >> 1, pq = q & 1;
+    float* xb = reinterpret_cast<float*>(staging) + pq * (2 * 2 * 32 * 16);
+    uint8_t* stg = SWIGLU ? staging + kXchgBytes + (warp - 2) * (16 * 32 * 2) : staging + (warp - 2) * (32 * 32 * 4);
+    uint32_t xseq = 0;  // exchange chunk counter (the same sequence in both warps of a pair)
+    bool ok = true;
     int n = 0;
-    for (int tile = first; tile < total; tile += stride, ++n) {
+    for (int tile = first; tile < total && ok; tile += stride, ++n) {
       const Tile t = decode_tile(a, sc, tile);
-      const int acc = n % a.acc_stages;
-      const uint32_t aph = (n / a.acc_stages) & 1;
+      const int acc = n & 1;
+      const uint32_t aph = (n >> 1) & 1;
       if (!mbar_wait(&tfull[acc], aph, a.err, kSiteGemmEpilogue)) break;
       tc_fence_after_sync();
       const SegDev& sg = a.seg[t.s];
       const uint32_t col0 = acc * a.acc_cols;
-      const int feat0 = t.mb * a.munit + (SPLIT ? 0 : static_cast<int>(rank) * kTileM) + q * 32;
       const int ncols = MOE_EXACT_N ? ((t.valid + 15) >> 4) << 4 : t.bn;  // the columns the MMA wrote
-      if constexpr (SPLIT) {
-        // Odd CTA: its TMEM holds the up projection of the pair's features;
-        // ship each 32-column chunk to the even CTA's exchange slot.  Even CTA:
-        // gate projection in TMEM, up arrives in the slot; finish
-        // SiLU(gate) * up and write h.  Slot rows are XOR-swizzled by lane.
-        bool ok = true;
-        for (int c0 = 0; c0 < ncols && ok; c0 += 32, ++cseq) {
+      if constexpr (SWIGLU) {
+        const bool own_gate = (half == 0) != (sg.up_first != 0);
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
+        __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stg);
+        // sub-tile u: features u*64.., accumulator at column u*bn_max
+        for (int u = 0; u < NSUB && ok; ++u) {
+          for (int c0 = 0; c0 < ncols; c0 += 32, ++xseq) {
+            const int feat0 = t.mb * a.munit + static_cast<int>(rank) * FEAT * NSUB + u * FEAT + pq * 32;
+            const int nc = min(32, ncols - c0);
+            uint32_t v[32];
+            const uint32_t ta = tmem_addr(tmem_base, q * 32, col0 + u * a.bn_max + c0);
+            if (nc == 32)
+              tmem_ld32(ta, v);
+            else
+              tmem_ld16(ta, v);
+            tmem_wait(v);
+            const int slot = xseq & 1;
+            float* send = xb + (slot * 2 + half) * (32 * 16) + lane * 16;
+            const float* recv = xb + (slot * 2 + (half ^ 1)) * (32 * 16) + lane * 16;
+            const int sw = (lane >> 1) & 3;  // 16-byte swizzle: conflict-free rows of 64 bytes
+            // Send the partner's 16 columns (none when the chunk has only 16 and
+            // this is the low-lane warp).
+            if (half == 1 || nc == 32) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                // constant register indices on both sides of the select
+                const uint4 lo = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+                const uint4 hi = make_uint4(v[16 + 4 * c], v[17 + 4 * c], v[18 + 4 * c], v[19 + 4 * c]);
+                *reinterpret_cast<uint4*>(send + 4 * (c ^ sw)) = half ? lo : hi;
+              }
+            }
+            mbar_arrive(&xfull[pq * 2 + slot]);
+            if (!mbar_wait(&xfull[pq * 2 + slot], (xseq >> 1) & 1, a.err, kSiteGemmEpilogue)) {
+              ok = false;
+              break;
+            }
+            const int my0 = half * 16;
+            if (my0 < nc) {
+              float p[16];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const float4 f = *reinterpret_cast<const float4*>(recv + 4 * (c ^ sw));
+                p[4 * c] = f.x;
+                p[4 * c + 1] = f.y;
+                p[4 * c + 2] = f.z;
+                p[4 * c + 3] = f.w;
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float own = __uint_as_float(half ? v[16 + j] : v[j]);
+                const float gv = own_gate ? own : p[j], uv = own_gate ? p[j] : own;
+                st[j * 32 + lane] = __float2bfloat16_rn(silu(gv) * uv);
+              }
+              __syncwarp();
+              for (int w = lane; w < 16 * 4; w += 32) {
+                const int j = w >> 2, piece = w & 3;
+                const int r = c0 + my0 + j;
+                const int row = t.b_row + r;
+                if (r < t.valid && row < sg.rows)
+                  *reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * sg.ldo + feat0 + piece * 8) =
+                      *reinterpret_cast<const uint4*>(st + j * 32 + piece * 8);
+              }
+              __syncwarp();
+            }
+          }
+        }
+      } else {
+        const int feat0 = t.mb * a.munit + static_cast<int>(rank) * FEAT + q * 32;
+        float* out = static_cast<float*>(sg.out) + t.out_off;
+        float* st = reinterpret_cast<float*>(stg);
+        for (int c0 = 0; c0 < ncols; c0 += 32) {
           const int nc = min(32, ncols - c0);
-          const int slot = cseq & 1;
-          const uint32_t xph = (cseq >> 1) & 1;
-          float* xrow = xbuf + ((q * 2 + slot) * 32 + lane) * 32;
           uint32_t g[32];
           const uint32_t ta = tmem_addr(tmem_base, q * 32, col0 + c0);
           if (nc == 32)
@@ -394,111 +494,19 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
           else
             tmem_ld16(ta, g);
           tmem_wait(g);
-          if (rank == 1) {
-            if (!mbar_wait(&xempty[q * 2 + slot], xph ^ 1, a.err, kSiteGemmEpilogue)) {
-              ok = false;
-              break;
-            }
-            const uint32_t rrow = mapa_shared(smem_u32(xrow), 0);
-            const uint32_t rbar = mapa_shared(smem_u32(&xfull[q * 2 + slot]), 0);
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              if (v < nc / 4) st_async_v4(rrow + ((v ^ (lane & 7)) << 4), g[4 * v], g[4 * v + 1], g[4 * v + 2], g[4 * v + 3], rbar);
-          } else {
-            if (lane == 0) mbar_arrive_expect_tx(&xfull[q * 2 + slot], nc * 32 * 4);
-            __syncwarp();
-            if (!mbar_wait(&xfull[q * 2 + slot], xph, a.err, kSiteGemmEpilogue)) {
-              ok = false;
-              break;
-            }
-            float u[32];
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              if (v < nc / 4) {
-                const float4 f = *reinterpret_cast<const float4*>(xrow + 4 * (v ^ (lane & 7)));
-                u[4 * v] = f.x;
-                u[4 * v + 1] = f.y;
-                u[4 * v + 2] = f.z;
-                u[4 * v + 3] = f.w;
-              }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&xempty[q * 2 + slot]), 1));
-            __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stg);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (j < nc) {
-                const float gv = __uint_as_float(g[j]);
-                st[j * 32 + lane] = __float2bfloat16_rn(silu(gv) * u[j]);
-              }
-            }
-            __syncwarp();
-            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
-            for (int v = lane; v < nc * 4; v += 32) {
-              const int j = v >> 2, piece = v & 3;
-              const int row = t.b_row + c0 + j;
-              if (c0 + j < t.valid && row < sg.rows)
-                *reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * sg.ldo + feat0 + piece * 8) =
-                    *reinterpret_cast<const uint4*>(st + j * 32 + piece * 8);
-            }
-            __syncwarp();
-          }
-        }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(tempty_leader + acc * 8);
-        if (!ok) break;
-        continue;
-      }
-      for (int c0 = 0; c0 < ncols; c0 += 32) {
-        const int nc = min(32, ncols - c0);
-        uint32_t g[32], u[32];
-        const uint32_t ta = tmem_addr(tmem_base, q * 32, col0 + c0);
-        if (nc == 32) {
-          tmem_ld32(ta, g);
-          if (NUM_A == 2) tmem_ld32(ta + a.bn_max, u);
-        } else {
-          tmem_ld16(ta, g);
-          if (NUM_A == 2) tmem_ld16(ta + a.bn_max, u);
-        }
-        if (NUM_A == 2)
-          tmem_wait(g, u);
-        else
-          tmem_wait(g);
-        if (EPI == kEpiSwiGLU) {
-          __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stg);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (j < nc) {
-              const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
-              st[j * 32 + lane] = __float2bfloat16_rn(silu(gv) * uv);
-            }
-          }
-          __syncwarp();
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
-          for (int v = lane; v < nc * 4; v += 32) {
-            const int j = v >> 2, piece = v & 3;
-            const int row = t.b_row + c0 + j;
-            if (c0 + j < t.valid && row < sg.rows)
-              *reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * sg.ldo + feat0 + piece * 8) =
-                  *reinterpret_cast<const uint4*>(st + j * 32 + piece * 8);
-          }
-        } else {
-          float* st = reinterpret_cast<float*>(stg);
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (j < nc) st[j * 32 + lane] = __uint_as_float(g[j]);
           __syncwarp();
-          float* out = static_cast<float*>(sg.out) + t.out_off;
-          for (int v = lane; v < nc * 8; v += 32) {
-            const int j = v >> 3, piece = v & 7;
+          for (int w = lane; w < nc * 8; w += 32) {
+            const int j = w >> 3, piece = w & 7;
             const int row = t.b_row + c0 + j;
             if (c0 + j < t.valid && row < sg.rows)
               *reinterpret_cast<float4*>(out + static_cast<size_t>(row) * sg.ldo + feat0 + piece * 4) =
                   *reinterpret_cast<const float4*>(st + j * 32 + piece * 4);
           }
+          __syncwarp();
         }
-        __syncwarp();
       }
       tc_fence_before_sync();
       __syncwarp();
@@ -522,16 +530,17 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
   }
 }
 
-template <int EPI>
+// NSUB: stacked 64-feature sub-tiles per CTA and tile (SwiGLU; 1 for the store).
+template <int EPI, int NSUB>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmMaps maps,
                                                                     const GemmArgs a) {
-  gemm_body<EPI, false>(maps, a);
+  gemm_body<EPI, false, NSUB>(maps, a);
 }
 
-template <int EPI>
+template <int EPI, int NSUB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
-  gemm_body<EPI, true>(maps, a);
+  gemm_body<EPI, true, NSUB>(maps, a);
 }
 
 template <typename K>
@@ -544,26 +553,18 @@ cudaError_t allow_big_smem(K kernel, bool* configured) {
   return e;
 }
 
-template <int EPI>
+template <int EPI, int NSUB>
 cudaError_t launch_epi(const GemmArgs& a, const GemmMaps& maps, int grid, size_t smem, bool pair,
                        cudaStream_t stream) {
   static bool single_ok[64] = {}, pair_ok[64] = {};
   cudaError_t e;
   if (pair) {
-    if ((e = allow_big_smem(grouped_gemm_pair_kernel<EPI>, pair_ok)) != cudaSuccess) return e;
-    grouped_gemm_pair_kernel<EPI><<<grid, kThreads, smem, stream>>>(maps, a);
+    if ((e = allow_big_smem(grouped_gemm_pair_kernel<EPI, NSUB>, pair_ok)) != cudaSuccess) return e;
+    grouped_gemm_pair_kernel<EPI, NSUB><<<grid, kThreads, smem, stream>>>(maps, a);
   } else {
-    if ((e = allow_big_smem(grouped_gemm_kernel<EPI>, single_ok)) != cudaSuccess) return e;
-    grouped_gemm_kernel<EPI><<<grid, kThreads, smem, stream>>>(maps, a);
+    if ((e = allow_big_smem(grouped_gemm_kernel<EPI, NSUB>, single_ok)) != cudaSuccess) return e;
+    grouped_gemm_kernel<EPI, NSUB><<<grid, kThreads, smem, stream>>>(maps, a);
   }
-  return cudaGetLastError();
-}
-
-cudaError_t launch_split(const GemmArgs& a, const GemmMaps& maps, int grid, size_t smem, cudaStream_t stream) {
-  static bool ok[64] = {};
-  cudaError_t e;
-  if ((e = allow_big_smem(grouped_gemm_pair_kernel<kEpiSwiGLUSplit>, ok)) != cudaSuccess) return e;
-  grouped_gemm_pair_kernel<kEpiSwiGLUSplit><<<grid, kThreads, smem, stream>>>(maps, a);
   return cudaGetLastError();
 }
 
@@ -573,7 +574,11 @@ uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
-constexpr int kFixedSmem = 1024 + kStagingBytes + static_cast<int>(sizeof(Sched)) + (2 * kMaxStages + 4 + 16) * 8 + 64;
+// Shared memory besides the pipeline stages: alignment slack, epilogue
+// staging, the schedule, the barriers and the TMEM address.
+constexpr int fixed_smem(int epi) {
+  return 1024 + staging_bytes(epi) + static_cast<int>(sizeof(Sched)) + (2 * kMaxStages + 4 + 4) * 8 + 64;
+}
 
 int bn_max_of(int num_segments, const GemmSegment* segs) {
   int m = 16;
@@ -584,48 +589,55 @@ int bn_max_of(int num_segments, const GemmSegment* segs) {
 }  // namespace
 
 // CTA pairs (tcgen05 cta_group::2) halve the token rows each CTA stages and
-// reads, which is what limits the large-tile, tensor-bound GEMMs; they need
-// weight blocks of 256 rows.  Measured on GB300: with 256-row token tiles the
-// down projection runs 18-20 % faster as pairs (Mixtral T=4096, DeepSeek-V3
-// T=8192); with 128-row or smaller tiles pairs gain nothing or lose a little.
+// reads, which is what limits the large-tile, tensor-bound GEMMs.  Measured on
+// GB300: with 256-row token tiles the down projection runs 18-20 % faster as
+// pairs (Mixtral T=4096, DeepSeek-V3 T=8192); with 128-row or smaller tiles
+// pairs gain nothing or lose a little.
 #ifndef MOE_PAIR_MIN_BN
 #define MOE_PAIR_MIN_BN 256
 #endif
-// The SwiGLU GEMM runs as split pairs (gate rows in the even CTA, up rows in
-// the odd one) when the token tiles of every segment reach this many rows
-// (0 = never).  Measured on GB300 it is slower than single CTAs (Mixtral
-// T=4096 gate+up 1600 vs 1467 us, DeepSeek-V3 T=8192 4423 vs 3794 us): the
-// per-chunk exchange through distributed shared memory costs more than the
-// operand traffic it saves.  Off by default.
-#ifndef MOE_SPLIT_MIN_BN
-#define MOE_SPLIT_MIN_BN 0
+// The same threshold for the SwiGLU GEMM, whose CTA holds 64 features: as a
+// pair, a token tile is read once per 128 features instead of once per 64.
+#ifndef MOE_PAIR_MIN_BN_SWIGLU
+#define MOE_PAIR_MIN_BN_SWIGLU 256
 #endif
-// Measured on GB300 (Mixtral-, Qwen2- and DeepSeek-V3-shaped layers): the
-// SwiGLU GEMM gains from 2-block stages even with only two stages once its
-// token tiles are >= 64 rows; the fp32-store GEMM needs three stages.
+// Largest number of 64-wide K blocks per pipeline stage (one 3-D / 4-D TMA
+// box each); taken when at least MOE_MIN_STAGES stages still fit.
 #ifndef MOE_KPS_MAX
 #define MOE_KPS_MAX 2
+#endif
+#ifndef MOE_MIN_STAGES
+#define MOE_MIN_STAGES 3
+#endif
+// SwiGLU: two stacked 64-feature sub-tiles per CTA while the token tile is at
+// most this many rows.  Small token tiles stream weights: two sub-tiles keep
+// more weight bytes per token byte in every stage (more weight bytes in
+// flight), and their two accumulators of bn columns still leave two slots in
+// TMEM.  At 256 rows one sub-tile keeps two accumulator slots.
+#ifndef MOE_NSUB2_MAX_BN
+#define MOE_NSUB2_MAX_BN 128
 #endif
 
 GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment* segs) {
   GemmPlan p{};
   const int bn_max = bn_max_of(num_segments, segs);
-  int bn_min = bn_max;
-  for (int s = 0; s < num_segments; ++s) bn_min = bn_min < segs[s].bn ? bn_min : segs[s].bn;
-  p.split = epi == kEpiSwiGLU && MOE_SPLIT_MIN_BN > 0 && bn_min >= MOE_SPLIT_MIN_BN;
-  p.pair = p.split || (MOE_PAIR_MIN_BN > 0 && bn_max >= MOE_PAIR_MIN_BN);
-  if (!p.split)
-    for (int s = 0; s < num_segments; ++s) p.pair = p.pair && segs[s].nout % (2 * kTileM) == 0;
-  const int num_a = (epi == kEpiSwiGLU && !p.split) ? 2 : 1;
-  const int per_kb = num_a * kATileBytes + (p.pair ? bn_max / 2 : bn_max) * kTileK * 2;
-  const int fixed = kFixedSmem + (p.split ? kXchgBytes : 0);
-  const int min_stages = (epi == kEpiSwiGLU && bn_max >= 64) ? 2 : 3;
+  const int feat = feat_per_cta(epi);
+  p.nsub = (epi == kEpiSwiGLU && bn_max <= MOE_NSUB2_MAX_BN) ? 2 : 1;
+  for (int s = 0; s < num_segments; ++s) p.nsub = segs[s].nout % (p.nsub * feat) == 0 ? p.nsub : 1;
+  const int pair_min = epi == kEpiSwiGLU ? MOE_PAIR_MIN_BN_SWIGLU : MOE_PAIR_MIN_BN;
+  p.pair = pair_min > 0 && bn_max >= pair_min;
+  for (int s = 0; s < num_segments; ++s) p.pair = p.pair && segs[s].nout % (2 * p.nsub * feat) == 0;
+  const int per_kb = p.nsub * kATileBytes + (p.pair ? bn_max / 2 : bn_max) * kTileK * 2;
+  // Two sub-tiles: two-block stages pay even with two stages once the token
+  // tiles reach 64 rows (measured on Mixtral-, Qwen2- and DeepSeek-V3-shaped layers).
+  const int min_stages = (p.nsub == 2 && bn_max >= 64) ? 2 : MOE_MIN_STAGES;
   p.kps = 1;
   for (int cand = 2; cand <= MOE_KPS_MAX; cand <<= 1) {
-    bool ok = (227 * 1024 - fixed) / (cand * per_kb) >= min_stages;
+    bool ok = (227 * 1024 - fixed_smem(epi)) / (cand * per_kb) >= min_stages;
     for (int s = 0; s < num_segments && ok; ++s) {
       const int ks = (epi == kEpiSwiGLU || segs[s].ksplit < 1) ? 1 : segs[s].ksplit;
       ok = segs[s].K % (kTileK * cand) == 0 && segs[s].K / (kTileK * cand) >= 2 * ks;
+      if (epi == kEpiSwiGLU && segs[s].a_mode == kTwoMaps) ok = false;  // two 2-D boxes per stage
     }
     if (ok) p.kps = cand;
   }
@@ -638,26 +650,25 @@ cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSe
   GemmArgs a{};
   a.nseg = num_segments;
   a.err = err;
-  a.munit = (plan.pair && !plan.split) ? 2 * kTileM : kTileM;
+  a.munit = feat_per_cta(epi) * plan.nsub * (plan.pair ? 2 : 1);
   long long upper = 0;
   for (int s = 0; s < num_segments; ++s) {
     const GemmSegment& g = segs[s];
     const int ks = (epi == kEpiSwiGLU || g.ksplit < 1) ? 1 : g.ksplit;
-    a.seg[s] = SegDev{g.offsets, g.groups, g.rows, g.nout, g.K, g.bn, g.ldo, ks, g.slice_stride, g.out};
+    a.seg[s] = SegDev{g.offsets, g.groups, g.rows, g.nout, g.K, g.bn, g.ldo, ks, g.a_mode, g.up_first,
+                      g.slice_stride, g.out};
     a.bn_max = a.bn_max > g.bn ? a.bn_max : g.bn;
     upper += static_cast<long long>(g.nout / a.munit) * ((g.rows + g.bn - 1) / g.bn + g.groups) * ks;
   }
-  const int num_a = (epi == kEpiSwiGLU && !plan.split) ? 2 : 1;
-  a.acc_cols = num_a * a.bn_max;
-  a.acc_stages = (2 * a.acc_cols <= 512) ? 2 : 1;
-  a.tmem_cols = static_cast<int>(pow2_at_least(static_cast<uint32_t>(a.acc_stages * a.acc_cols)));
+  a.acc_cols = plan.nsub * a.bn_max;
+  a.tmem_cols = static_cast<int>(pow2_at_least(static_cast<uint32_t>(2 * a.acc_cols)));
   a.kps = plan.kps;
-  const int stage_bytes = a.kps * (num_a * kATileBytes + (plan.pair ? a.bn_max / 2 : a.bn_max) * kTileK * 2);
-  const int fixed = kFixedSmem + (plan.split ? kXchgBytes : 0);
-  int stages = (227 * 1024 - fixed) / stage_bytes;
+  const int stage_bytes =
+      a.kps * (plan.nsub * kATileBytes + (plan.pair ? a.bn_max / 2 : a.bn_max) * kTileK * 2);
+  int stages = (227 * 1024 - fixed_smem(epi)) / stage_bytes;
   if (stages > kMaxStages) stages = kMaxStages;
   a.stages = stages;
-  const size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(stages) * stage_bytes;
+  const size_t smem = static_cast<size_t>(fixed_smem(epi)) + static_cast<size_t>(stages) * stage_bytes;
   int units = plan.pair ? num_sms / 2 : num_sms;  // CTAs, or CTA pairs
   if (upper < units) units = static_cast<int>(upper);
   if (units < 1) units = 1;
@@ -665,9 +676,11 @@ cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSe
   GemmMaps maps;
   maps.seg[0] = seg_maps[0];
   maps.seg[1] = seg_maps[num_segments > 1 ? 1 : 0];
-  if (plan.split) return launch_split(a, maps, grid, smem, stream);
-  if (epi == kEpiSwiGLU) return launch_epi<kEpiSwiGLU>(a, maps, grid, smem, plan.pair, stream);
-  return launch_epi<kEpiStoreF32>(a, maps, grid, smem, plan.pair, stream);
+  if (epi == kEpiSwiGLU) {
+    if (plan.nsub == 2) return launch_epi<kEpiSwiGLU, 2>(a, maps, grid, smem, plan.pair, stream);
+    return launch_epi<kEpiSwiGLU, 1>(a, maps, grid, smem, plan.pair, stream);
+  }
+  return launch_epi<kEpiStoreF32, 1>(a, maps, grid, smem, plan.pair, stream);
 }
 
 }  // namespace moe

@@ -45,6 +45,14 @@ cudaError_t launch_permute(const int32_t* topk_idx, const void* x, int T, int H,
                            int32_t* offsets, int32_t* perm, int32_t* inv, void* x_perm, void* scratch,
                            uint32_t* err, cudaStream_t stream);
 
+// How the SwiGLU GEMM loads its A tile (64 gate rows over the 64 up rows of
+// the same features).  kStackedMap: one TMA box over a view whose extra
+// dimension steps from the gate to the up weights (its stride is the distance
+// between the two tensors); kTwoMaps: two 64-row boxes, one per tensor, used
+// when that distance cannot be a TMA stride (it must be a non-zero multiple
+// of 16 bytes below 2^40); one K block per stage.
+enum SwiGLULoad { kStackedMap = 0, kTwoMaps = 1 };
+
 // One operand set of the grouped GEMM: groups of rows of B against
 // per-group weight blocks of A.
 struct GemmSegment {
@@ -59,32 +67,34 @@ struct GemmSegment {
   int ksplit = 1;          // plain store only: K cut into ksplit slices, slice s of
                            // the partial sums goes to out + s * slice_stride
   size_t slice_stride = 0; // elements
+  int a_mode = kStackedMap;  // SwiGLU only
+  int up_first = 0;          // SwiGLU, kStackedMap: the view's first plane is the up weights
 };
 
-// kEpiSwiGLU: two accumulators (gate, up) per CTA.  kEpiSwiGLUSplit: CTA
-// pairs only; the pair's M=256 MMA puts 128 gate rows in the even CTA and the
-// matching 128 up rows in the odd CTA, which streams its up values to the
-// even CTA through distributed shared memory.  kEpiStoreF32: one accumulator,
-// fp32 out.
-enum GemmEpilogue { kEpiSwiGLU = 0, kEpiStoreF32 = 1, kEpiSwiGLUSplit = 2 };
+// kEpiSwiGLU: gate and up rows stacked in one A tile, h = SiLU(gate) * up
+// in bf16.  kEpiStoreF32: one accumulator, fp32 out.
+enum GemmEpilogue { kEpiSwiGLU = 0, kEpiStoreF32 = 1 };
 
 // How the grouped GEMM will run these segments: as CTA pairs (tcgen05
-// cta_group::2, 256-row weight tiles; each CTA stages bn/2 token rows) or
-// single CTAs, and with how many 64-wide K blocks per pipeline stage.  The A
-// maps and the token map must be built to match (token box bn/2 rows for a
-// pair; box depth kps).
+// cta_group::2; each CTA stages bn/2 token rows) or single CTAs, and with how
+// many 64-wide K blocks per pipeline stage.  The maps must be built to match
+// (token box bn/2 rows for a pair; box depth kps).
 struct GemmPlan {
   bool pair;
-  bool split;  // SwiGLU as split pairs (kEpiSwiGLUSplit); implies pair
   int kps;
+  int nsub;  // SwiGLU: stacked 64-feature sub-tiles per CTA and tile (1 or 2); 1 otherwise
 };
 GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment* segs);
 
-// TMA descriptors of one grouped-GEMM segment.  a0 / a1 cover the
-// [groups*nout, K] weights (gate and up for SwiGLU; a1 unused otherwise) with
-// box 128 rows x 64 columns; b covers the [rows, K] token rows with box bn
-// rows x 64 columns.  With kps > 1 they are 3-D views {64, rows, K/64} with
-// box depth kps.
+// TMA descriptors of one grouped-GEMM segment; b covers the [rows, K] token
+// rows with box {64 columns, bn (or bn/2) rows}, as a 3-D view {64, rows,
+// K/64} with box depth kps when kps > 1.
+//   Store:  a0 covers the [groups*nout, K] weights, box 128 rows.
+//   SwiGLU, kStackedMap: a0 is the view {K, groups*nout, 2} (kps == 1) or
+//           {64, groups*nout, 2, K/64} (kps > 1) of the gate and up weights
+//           (plane stride = the distance between them), box 64 rows x 2
+//           planes (x kps); one box per 64-feature sub-tile.
+//   SwiGLU, kTwoMaps: a0 / a1 cover the gate / up weights, box 64 rows.
 struct SegMaps {
   CUtensorMap a0, a1, b;
 };

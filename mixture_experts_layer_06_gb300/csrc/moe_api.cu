@@ -116,6 +116,46 @@ bool make_gemm_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
   return kps == 1 ? make_map(m, base, rows, cols, box_rows) : make_map3d(m, base, rows, cols, box_rows, kps);
 }
 
+// Stacked view of a SwiGLU segment's gate and up weights (both bf16
+// [rows, K] row-major): one more dimension of extent 2 whose stride is the
+// distance between the two tensors, lower address first, so that one box
+// {64 columns, 64 rows, 2 planes} lands as 64 gate rows over the 64 up rows
+// of the same features: one 128-row A tile.  With kps > 1 it is the 4-D view
+// {64, rows, 2, K/64}, box depth kps (kps such tiles, one per K block).
+// (A 5-D view that also spans consecutive 64-row blocks in one box measured
+// far slower on GB300 than one 4-D box per block.)  Fails when the distance
+// cannot be a TMA stride.
+bool stackable(const void* w_gate, const void* w_up) {
+  const uint64_t g = reinterpret_cast<uintptr_t>(w_gate), u = reinterpret_cast<uintptr_t>(w_up);
+  const uint64_t dist = g < u ? u - g : g - u;
+  return dist != 0 && dist % 16 == 0 && dist < (1ull << 40);
+}
+
+bool make_stacked_map(CUtensorMap* m, const void* w_gate, const void* w_up, uint64_t rows, uint64_t K, int kps,
+                      int* up_first) {
+  if (!stackable(w_gate, w_up)) return false;
+  const uint64_t g = reinterpret_cast<uintptr_t>(w_gate), u = reinterpret_cast<uintptr_t>(w_up);
+  *up_first = u < g ? 1 : 0;
+  void* base = const_cast<void*>(u < g ? w_up : w_gate);
+  const uint64_t dist = u < g ? g - u : u - g;
+  if (kps == 1) {
+    const cuuint64_t dims[3] = {K, rows, 2};
+    const cuuint64_t strides[2] = {K * 2, dist};
+    const cuuint32_t box[3] = {64, 64, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  const cuuint64_t dims[4] = {64, rows, 2, K / 64};
+  const cuuint64_t strides[3] = {K * 2, dist, 128};
+  const cuuint32_t box[4] = {64, 64, 2, static_cast<cuuint32_t>(kps)};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 moe_status_t check_dims(int T, int H, int F, int E, int k) {
@@ -157,14 +197,6 @@ moe::RouteSpec route_spec(const moe_config_t& c) {
   s.logit_bias = c.logit_bias;
   return s;
 }
-
-// Token tile of the SwiGLU GEMM for a segment: as for the down GEMM, the
-// smallest of 16..256 covering the mean rows per group.  With 256-row tiles the
-// two accumulators fill TMEM (one stage, the epilogue does not overlap the
-// next tile), but each MMA moves the fewest operand bytes per flop; measured
-// on GB300 this beats 128-row tiles with two stages (Mixtral T=4096 gate+up
-// 1432 vs 1465 us).
-int swiglu_bn(long long rows, int groups);
 
 // Token tile of the grouped GEMM: the smallest of 16..bn_max that covers the
 // mean rows per group.
@@ -211,8 +243,6 @@ Split choose_split(const moe_config_t& c, int T, int H, int F, int E, int k) {
   }
   return sp;
 }
-
-int swiglu_bn(long long rows, int groups) { return choose_bn(rows, groups, 256); }
 
 // Token tile of a dense shared-expert segment that shares a launch with the
 // routed segment: no larger than the routed tile (or 128), so that it does not
@@ -299,18 +329,31 @@ moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStre
   // gate+up: B = token rows [rows, H], A = gate / up weights [groups*F, H]
   for (int s = 0; s < nseg; ++s) {
     const FfnOperands& o = ops[s];
-    const int bn = (nseg > 1 && s == 1) ? shared_bn(o.rows, seg[0].bn) : swiglu_bn(o.rows, o.groups);
+    const int bn = (nseg > 1 && s == 1) ? shared_bn(o.rows, seg[0].bn) : choose_bn(o.rows, o.groups);
     seg[s] = GemmSegment{o.offsets, o.groups, o.rows, o.F, o.H, bn, o.h, o.F};
+    seg[s].a_mode = stackable(o.w_gate, o.w_up) ? moe::kStackedMap : moe::kTwoMaps;
   }
-  moe::GemmPlan plan = moe::grouped_gemm_plan(moe::kEpiSwiGLU, nseg, seg);
-  for (int s = 0; s < nseg; ++s) {
-    const FfnOperands& o = ops[s];
-    const uint64_t wrows = static_cast<uint64_t>(o.groups) * o.F;
-    const uint32_t brows = plan.pair ? seg[s].bn / 2 : seg[s].bn;
-    if (!make_gemm_map(&maps[s].a0, o.w_gate, wrows, o.H, 128, plan.kps) ||
-        !make_gemm_map(&maps[s].a1, o.w_up, wrows, o.H, 128, plan.kps) ||
-        !make_gemm_map(&maps[s].b, o.x_rows, o.rows, o.H, brows, plan.kps))
-      return MOE_ERR_CUDA;
+  for (int attempt = 0;; ++attempt) {
+    const moe::GemmPlan plan = moe::grouped_gemm_plan(moe::kEpiSwiGLU, nseg, seg);
+    bool replan = false;
+    for (int s = 0; s < nseg && !replan; ++s) {
+      const FfnOperands& o = ops[s];
+      const uint64_t wrows = static_cast<uint64_t>(o.groups) * o.F;
+      const uint32_t brows = plan.pair ? seg[s].bn / 2 : seg[s].bn;
+      if (seg[s].a_mode == moe::kStackedMap) {
+        if (!make_stacked_map(&maps[s].a0, o.w_gate, o.w_up, wrows, o.H, plan.kps, &seg[s].up_first)) {
+          if (attempt > 0) return MOE_ERR_CUDA;
+          seg[s].a_mode = moe::kTwoMaps;  // fall back to two boxes per stage
+          replan = true;
+          continue;
+        }
+        maps[s].a1 = maps[s].a0;
+      } else if (!make_map(&maps[s].a0, o.w_gate, wrows, o.H, 64) || !make_map(&maps[s].a1, o.w_up, wrows, o.H, 64)) {
+        return MOE_ERR_CUDA;
+      }
+      if (!make_gemm_map(&maps[s].b, o.x_rows, o.rows, o.H, brows, plan.kps)) return MOE_ERR_CUDA;
+    }
+    if (!replan) break;
   }
   if (moe::launch_grouped_gemm(moe::kEpiSwiGLU, nseg, seg, maps, d->num_sms, d->err, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -321,7 +364,7 @@ moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStre
     seg[s] = GemmSegment{o.offsets, o.groups, o.rows, o.H, o.F, bn, o.y, o.H, o.ksplit,
                          static_cast<size_t>(o.rows) * o.H};
   }
-  plan = moe::grouped_gemm_plan(moe::kEpiStoreF32, nseg, seg);
+  const moe::GemmPlan plan = moe::grouped_gemm_plan(moe::kEpiStoreF32, nseg, seg);
   for (int s = 0; s < nseg; ++s) {
     const FfnOperands& o = ops[s];
     const uint64_t wrows = static_cast<uint64_t>(o.groups) * o.H;

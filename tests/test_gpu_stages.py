@@ -165,6 +165,46 @@ def test_expert_ffn(name, counts, H, F):
     assert np.abs(y_gpu - y_or).max() <= 1e-2 * np.abs(y_or).max()
 
 
+@pytest.mark.parametrize("counts,H,F", [([5, 17, 1, 30], 256, 384), ([300, 257, 200, 255], 512, 512)],
+                         ids=["small_tiles", "pair_tiles"])
+def test_expert_ffn_weight_placement(counts, H, F):
+    """The gate+up GEMM loads 64 gate rows and the 64 up rows of the same
+    features as one tile, through a view whose extra dimension steps from one
+    weight tensor to the other.  The result must not depend on where the two
+    tensors lie: gate below up, up below gate, or one tensor passed as both
+    (the view cannot be formed; two loads per tile)."""
+    xp, offsets, wg, wu, wd = _ffn_case(counts, H, F)
+    n = wg.size
+    x_d, off_d, wd_d = dev_bf16(xp), dev_i32(offsets), dev_bf16(wd)
+    gate_low = dev_bf16(np.concatenate([wg.reshape(-1), wu.reshape(-1)]))
+    up_low = dev_bf16(np.concatenate([wu.reshape(-1), wg.reshape(-1)]))
+    runs = {
+        "gate_below_up": (gate_low[:n].view(wg.shape), gate_low[n:].view(wu.shape)),
+        "up_below_gate": (up_low[n:].view(wg.shape), up_low[:n].view(wu.shape)),
+    }
+    outs = {}
+    for name, (g_d, u_d) in runs.items():
+        assert (g_d.data_ptr() < u_d.data_ptr()) == (name == "gate_below_up")
+        outs[name] = moe.moe_expert_ffn(x_d, off_d, g_d, u_d, wd_d)
+        assert moe.moe_device_error()[0] == 0
+    h_or, y_or = _oracle_ffn(xp, offsets, wg, wu, wd)
+    for name, (h, y) in outs.items():
+        h_gpu, y_gpu = host_f64(h), host_f64(y)
+        assert np.all(np.abs(h_gpu - h_or) <= 2.0 ** -8 * np.abs(h_or) + 1e-4), name
+        assert np.linalg.norm(y_gpu - y_or) / np.linalg.norm(y_or) < 4e-3, name
+    # the same dot products in the same order: bitwise equal
+    assert torch.equal(outs["gate_below_up"][0], outs["up_below_gate"][0])
+    assert torch.equal(outs["gate_below_up"][1], outs["up_below_gate"][1])
+    # one tensor as gate and up: h = SiLU(g) * g
+    g_d = gate_low[:n].view(wg.shape)
+    h, y = moe.moe_expert_ffn(x_d, off_d, g_d, g_d, wd_d)
+    assert moe.moe_device_error()[0] == 0
+    h_or, y_or = _oracle_ffn(xp, offsets, wg, wg, wd)
+    h_gpu, y_gpu = host_f64(h), host_f64(y)
+    assert np.all(np.abs(h_gpu - h_or) <= 2.0 ** -8 * np.abs(h_or) + 1e-4)
+    assert np.linalg.norm(y_gpu - y_or) / np.linalg.norm(y_or) < 4e-3
+
+
 def test_dense_ffn_matches_plain_swiglu():
     xp, _, wg, wu, wd = _ffn_case([200], 512, 768)
     h, y = moe.moe_expert_ffn(dev_bf16(xp), None, dev_bf16(wg[0]), dev_bf16(wu[0]), dev_bf16(wd[0]))
