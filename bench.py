@@ -153,6 +153,20 @@ def stage_algorithmic(wl, active: int):
     return out
 
 
+def workload_overrides(args) -> dict:
+    """Per-run changes to the named layer shape: the Zipf exponent, and a
+    reduced expert count (--experts) that keeps H, F, k and the routing
+    variant (groups of E / n_group experts) for small profiling captures; the
+    label names the expert count, so such a line is never the headline."""
+    kw = {} if args.alpha is None else {"alpha": args.alpha}
+    if args.experts is not None:
+        base = synth.workload(args.workload)
+        if args.experts < base.k or args.experts % base.n_group != 0:
+            raise SystemExit(f"--experts must be >= k={base.k} and a multiple of n_group={base.n_group}")
+        kw["E"] = args.experts
+    return kw
+
+
 def sources_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mixture_experts_layer_06_gb300", "csrc")
@@ -191,7 +205,7 @@ def run_ours(args):
     moe.load_library()
     stream = torch.cuda.current_stream()
 
-    kw = {} if args.alpha is None else {"alpha": args.alpha}
+    kw = workload_overrides(args)
     T_main = args.T if args.T is not None else max(T_SWEEP[args.workload])
     sweep_T = [] if args.no_sweep else [t for t in T_SWEEP[args.workload] if t != T_main]
     T_all = max([T_main] + sweep_T)
@@ -416,7 +430,7 @@ def run_reference(args):
         return
     import oracle
 
-    kw = {} if args.alpha is None else {"alpha": args.alpha}
+    kw = workload_overrides(args)
     T = args.T if args.T is not None else max(T_SWEEP[args.workload])
     wl = synth.workload(args.workload, T=T, **kw)
     inp = synth.make_inputs(wl)
@@ -453,6 +467,8 @@ def main():
     ap.add_argument("--workload", default="mixtral", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--alpha", type=float, default=None)
+    ap.add_argument("--experts", type=int, default=None,
+                    help="reduced expert count (same H, F, k, routing) for small profiling captures")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

@@ -296,10 +296,13 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
                   tma_load_4d_pair(dst, &ms.a0, bar, 0, a_row + u * kHalfRows, 0, kb * KPS);
               }
             } else {
-              if (KPS == 1)
-                tma_load_2d_pair(st, &ms.a0, bar, kb * kTileK, a_row);
-              else
-                tma_load_3d_pair(st, &ms.a0, bar, 0, a_row, kb * KPS);
+              for (int u = 0; u < NSUB; ++u) {  // sub-tile u: 128 weight rows, KPS * 16 KB
+                uint8_t* dst = st + u * KPS * kATileBytes;
+                if (KPS == 1)
+                  tma_load_2d_pair(dst, &ms.a0, bar, kb * kTileK, a_row + u * kTileM);
+                else
+                  tma_load_3d_pair(dst, &ms.a0, bar, 0, a_row + u * kTileM, kb * KPS);
+              }
             }
             if (KPS == 1)
               tma_load_2d_pair(sb, &ms.b, bar, kb * kTileK, b_row);
@@ -321,10 +324,13 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
                   tma_load_4d(dst, &ms.a0, &full[s], 0, a_row + u * kHalfRows, 0, kb * KPS);
               }
             } else {
-              if (KPS == 1)
-                tma_load_2d(st, &ms.a0, &full[s], kb * kTileK, a_row);
-              else
-                tma_load_3d(st, &ms.a0, &full[s], 0, a_row, kb * KPS);
+              for (int u = 0; u < NSUB; ++u) {
+                uint8_t* dst = st + u * KPS * kATileBytes;
+                if (KPS == 1)
+                  tma_load_2d(dst, &ms.a0, &full[s], kb * kTileK, a_row + u * kTileM);
+                else
+                  tma_load_3d(dst, &ms.a0, &full[s], 0, a_row + u * kTileM, kb * KPS);
+              }
             }
             if (KPS == 1)
               tma_load_2d(sb, &ms.b, &full[s], kb * kTileK, b_row);
@@ -482,30 +488,33 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
           }
         }
       } else {
-        const int feat0 = t.mb * a.munit + static_cast<int>(rank) * FEAT + q * 32;
         float* out = static_cast<float*>(sg.out) + t.out_off;
         float* st = reinterpret_cast<float*>(stg);
-        for (int c0 = 0; c0 < ncols; c0 += 32) {
-          const int nc = min(32, ncols - c0);
-          uint32_t g[32];
-          const uint32_t ta = tmem_addr(tmem_base, q * 32, col0 + c0);
-          if (nc == 32)
-            tmem_ld32(ta, g);
-          else
-            tmem_ld16(ta, g);
-          tmem_wait(g);
+        // sub-tile u: weight rows u*128.., accumulator at column u*bn_max
+        for (int u = 0; u < NSUB; ++u) {
+          const int feat0 = t.mb * a.munit + static_cast<int>(rank) * FEAT * NSUB + u * FEAT + q * 32;
+          for (int c0 = 0; c0 < ncols; c0 += 32) {
+            const int nc = min(32, ncols - c0);
+            uint32_t g[32];
+            const uint32_t ta = tmem_addr(tmem_base, q * 32, col0 + u * a.bn_max + c0);
+            if (nc == 32)
+              tmem_ld32(ta, g);
+            else
+              tmem_ld16(ta, g);
+            tmem_wait(g);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nc) st[j * 32 + lane] = __uint_as_float(g[j]);
-          __syncwarp();
-          for (int w = lane; w < nc * 8; w += 32) {
-            const int j = w >> 3, piece = w & 7;
-            const int row = t.b_row + c0 + j;
-            if (c0 + j < t.valid && row < sg.rows)
-              *reinterpret_cast<float4*>(out + static_cast<size_t>(row) * sg.ldo + feat0 + piece * 4) =
-                  *reinterpret_cast<const float4*>(st + j * 32 + piece * 4);
+            for (int j = 0; j < 32; ++j)
+              if (j < nc) st[j * 32 + lane] = __uint_as_float(g[j]);
+            __syncwarp();
+            for (int w = lane; w < nc * 8; w += 32) {
+              const int j = w >> 3, piece = w & 7;
+              const int row = t.b_row + c0 + j;
+              if (c0 + j < t.valid && row < sg.rows)
+                *reinterpret_cast<float4*>(out + static_cast<size_t>(row) * sg.ldo + feat0 + piece * 4) =
+                    *reinterpret_cast<const float4*>(st + j * 32 + piece * 4);
+            }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
       tc_fence_before_sync();
@@ -530,7 +539,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
   }
 }
 
-// NSUB: stacked 64-feature sub-tiles per CTA and tile (SwiGLU; 1 for the store).
+// NSUB: sub-tiles per CTA and tile (SwiGLU: stacked 64-feature tiles; store: 128-row tiles).
 template <int EPI, int NSUB>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmMaps maps,
                                                                     const GemmArgs a) {
@@ -609,28 +618,69 @@ int bn_max_of(int num_segments, const GemmSegment* segs) {
 #ifndef MOE_MIN_STAGES
 #define MOE_MIN_STAGES 3
 #endif
-// SwiGLU: two stacked 64-feature sub-tiles per CTA while the token tile is at
-// most this many rows.  Small token tiles stream weights: two sub-tiles keep
-// more weight bytes per token byte in every stage (more weight bytes in
-// flight), and their two accumulators of bn columns still leave two slots in
-// TMEM.  At 256 rows one sub-tile keeps two accumulator slots.
-#ifndef MOE_NSUB2_MAX_BN
-#define MOE_NSUB2_MAX_BN 128
+// Sub-tiles per CTA and tile (NSUB).  Small token tiles stream weights: two
+// sub-tiles put more weight bytes per token byte into every stage (more
+// weight bytes in flight per SM), and 2 x NSUB accumulators of bn columns
+// must fit in TMEM's 512 columns, so 256-row tiles take one.  Measured on
+// GB300: two sub-tiles gain 6-14 % on the SwiGLU GEMM at 128-row tiles and
+// 8-11 % on the down projection at 64-128-row tiles (Mixtral-, Qwen2-,
+// DeepSeek-V3-shaped layers).  But halving the tile count can leave a last
+// wave of tiles on few SMs (Mixtral T=1: 224 tiles on 152 SMs), so two
+// sub-tiles are taken only while the expected tiles still fill their waves.
+#ifndef MOE_NSUB_SMALL
+#define MOE_NSUB_SMALL 2  // token tiles of 16..128 rows
+#endif
+#ifndef MOE_MIN_WAVE_FILL
+#define MOE_MIN_WAVE_FILL 0.9
 #endif
 
-GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment* segs) {
+namespace {
+
+// Sub-tiles the plan starts from for token tiles of bn_max rows.
+int gemm_nsub(int bn_max) {
+  int n = bn_max >= 256 ? 1 : MOE_NSUB_SMALL;
+  while (n > 1 && 2 * n * bn_max > 512) n >>= 1;
+  return n;
+}
+
+// Expected tiles of a launch (host estimate from the shapes: rows spread
+// evenly over min(groups, rows) groups) and the fill of its last wave.
+double wave_fill(GemmEpilogue epi, int num_segments, const GemmSegment* segs, int munit, int units) {
+  long long tiles = 0;
+  for (int s = 0; s < num_segments; ++s) {
+    const GemmSegment& g = segs[s];
+    const long long active = g.offsets == nullptr ? 1 : (g.rows < g.groups ? g.rows : g.groups);
+    if (active <= 0) continue;
+    const long long per = (g.rows + active - 1) / active;
+    const int ks = (epi == kEpiSwiGLU || g.ksplit < 1) ? 1 : g.ksplit;
+    tiles += active * ((per + g.bn - 1) / g.bn) * (g.nout / munit) * ks;
+  }
+  if (tiles <= 0 || units <= 0) return 1.0;
+  const long long waves = (tiles + units - 1) / units;
+  return static_cast<double>(tiles) / static_cast<double>(waves * units);
+}
+
+}  // namespace
+
+GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment* segs, int num_sms) {
   GemmPlan p{};
   const int bn_max = bn_max_of(num_segments, segs);
   const int feat = feat_per_cta(epi);
-  p.nsub = (epi == kEpiSwiGLU && bn_max <= MOE_NSUB2_MAX_BN) ? 2 : 1;
-  for (int s = 0; s < num_segments; ++s) p.nsub = segs[s].nout % (p.nsub * feat) == 0 ? p.nsub : 1;
+  p.nsub = gemm_nsub(bn_max);
+  for (int s = 0; s < num_segments; ++s)
+    while (p.nsub > 1 && segs[s].nout % (p.nsub * feat) != 0) p.nsub >>= 1;
   const int pair_min = epi == kEpiSwiGLU ? MOE_PAIR_MIN_BN_SWIGLU : MOE_PAIR_MIN_BN;
   p.pair = pair_min > 0 && bn_max >= pair_min;
   for (int s = 0; s < num_segments; ++s) p.pair = p.pair && segs[s].nout % (2 * p.nsub * feat) == 0;
+  if (p.nsub > 1 && !p.pair) {
+    const double fill = wave_fill(epi, num_segments, segs, feat * p.nsub, num_sms);
+    if (fill < MOE_MIN_WAVE_FILL && wave_fill(epi, num_segments, segs, feat, num_sms) > fill) p.nsub = 1;
+  }
   const int per_kb = p.nsub * kATileBytes + (p.pair ? bn_max / 2 : bn_max) * kTileK * 2;
-  // Two sub-tiles: two-block stages pay even with two stages once the token
-  // tiles reach 64 rows (measured on Mixtral-, Qwen2- and DeepSeek-V3-shaped layers).
-  const int min_stages = (p.nsub == 2 && bn_max >= 64) ? 2 : MOE_MIN_STAGES;
+  // Several sub-tiles: two-block stages pay even with two stages once the
+  // token tiles reach 64 rows (measured on Mixtral-, Qwen2- and
+  // DeepSeek-V3-shaped layers).
+  const int min_stages = (p.nsub >= 2 && bn_max >= 64) ? 2 : MOE_MIN_STAGES;
   p.kps = 1;
   for (int cand = 2; cand <= MOE_KPS_MAX; cand <<= 1) {
     bool ok = (227 * 1024 - fixed_smem(epi)) / (cand * per_kb) >= min_stages;
@@ -646,7 +696,7 @@ GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment
 
 cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSegment* segs, const SegMaps* seg_maps,
                                 int num_sms, uint32_t* err, cudaStream_t stream) {
-  const GemmPlan plan = grouped_gemm_plan(epi, num_segments, segs);
+  const GemmPlan plan = grouped_gemm_plan(epi, num_segments, segs, num_sms);
   GemmArgs a{};
   a.nseg = num_segments;
   a.err = err;
@@ -680,6 +730,7 @@ cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSe
     if (plan.nsub == 2) return launch_epi<kEpiSwiGLU, 2>(a, maps, grid, smem, plan.pair, stream);
     return launch_epi<kEpiSwiGLU, 1>(a, maps, grid, smem, plan.pair, stream);
   }
+  if (plan.nsub == 2) return launch_epi<kEpiStoreF32, 2>(a, maps, grid, smem, plan.pair, stream);
   return launch_epi<kEpiStoreF32, 1>(a, maps, grid, smem, plan.pair, stream);
 }
 

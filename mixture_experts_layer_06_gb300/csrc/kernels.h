@@ -82,9 +82,9 @@ enum GemmEpilogue { kEpiSwiGLU = 0, kEpiStoreF32 = 1 };
 struct GemmPlan {
   bool pair;
   int kps;
-  int nsub;  // SwiGLU: stacked 64-feature sub-tiles per CTA and tile (1 or 2); 1 otherwise
+  int nsub;  // sub-tiles per CTA and tile (1 or 2; see gemm_nsub)
 };
-GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment* segs);
+GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment* segs, int num_sms);
 
 // TMA descriptors of one grouped-GEMM segment; b covers the [rows, K] token
 // rows with box {64 columns, bn (or bn/2) rows}, as a 3-D view {64, rows,

@@ -334,7 +334,7 @@ moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStre
     seg[s].a_mode = stackable(o.w_gate, o.w_up) ? moe::kStackedMap : moe::kTwoMaps;
   }
   for (int attempt = 0;; ++attempt) {
-    const moe::GemmPlan plan = moe::grouped_gemm_plan(moe::kEpiSwiGLU, nseg, seg);
+    const moe::GemmPlan plan = moe::grouped_gemm_plan(moe::kEpiSwiGLU, nseg, seg, d->num_sms);
     bool replan = false;
     for (int s = 0; s < nseg && !replan; ++s) {
       const FfnOperands& o = ops[s];
@@ -364,7 +364,7 @@ moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStre
     seg[s] = GemmSegment{o.offsets, o.groups, o.rows, o.H, o.F, bn, o.y, o.H, o.ksplit,
                          static_cast<size_t>(o.rows) * o.H};
   }
-  const moe::GemmPlan plan = moe::grouped_gemm_plan(moe::kEpiStoreF32, nseg, seg);
+  const moe::GemmPlan plan = moe::grouped_gemm_plan(moe::kEpiStoreF32, nseg, seg, d->num_sms);
   for (int s = 0; s < nseg; ++s) {
     const FfnOperands& o = ops[s];
     const uint64_t wrows = static_cast<uint64_t>(o.groups) * o.H;
