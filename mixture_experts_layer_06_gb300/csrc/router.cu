@@ -211,33 +211,73 @@ __global__ void router_topk_kernel(const TopkArgs a) {
   auto score = [&](float v) { return sigmoid ? 1.f / (1.f + __expf(-v)) : __expf(v - mx) * inv_se; };
 
   // Group limiting: group score = sum of its top group_topn scores; keep the
-  // topk_group best groups (lane g holds group g's score).
+  // topk_group best groups (lane g holds group g's score).  Scores and group
+  // ids are computed once per column.
   const int gsize = a.spec.n_group > 1 ? E / a.spec.n_group : E;
   uint32_t kept = 0xFFFFFFFFu;
+  int gid[kJMax];
   if (a.spec.n_group > 1) {
+    float sc[kJMax];
+#pragma unroll
+    for (int j = 0; j < kJMax; ++j) {
+      const int c = lane + 32 * j;
+      sc[j] = c < E ? score(l[j]) : -INFINITY;
+      gid[j] = c < E ? c / gsize : -1;  // no group
+    }
     float my_gscore = -INFINITY;
-    for (int g = 0; g < a.spec.n_group; ++g) {
-      uint32_t taken = 0;
-      float sum = 0.f;
-      for (int r = 0; r < a.spec.group_topn; ++r) {
-        float v = -INFINITY;
-        int i = INT_MAX;
+    if (gsize % 32 == 0 && a.spec.group_topn <= 2) {
+      // Group g is the columns j in [g*gpj, (g+1)*gpj) of every lane: each
+      // lane takes its own best two, then a butterfly merges the pairs
+      // (disjoint lane sets at every step, so nothing is counted twice).
+      const int gpj = gsize / 32;
+      for (int g = 0; g < a.spec.n_group; ++g) {
+        float b1 = -INFINITY, b2 = -INFINITY;
 #pragma unroll
         for (int j = 0; j < kJMax; ++j) {
-          const int c = lane + 32 * j;
-          if (c < E && c / gsize == g && !((taken >> j) & 1u)) {
-            const float sc = score(l[j]);
-            if (sc > v || (sc == v && c < i)) {
-              v = sc;
-              i = c;
+          if (j >= g * gpj && j < (g + 1) * gpj) {
+            const float v = sc[j];
+            if (v > b1) {
+              b2 = b1;
+              b1 = v;
+            } else if (v > b2) {
+              b2 = v;
             }
           }
         }
-        warp_best(v, i);
-        sum += v;
-        if (i != INT_MAX && (i & 31) == lane) taken |= 1u << (i >> 5);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float p1 = __shfl_xor_sync(0xFFFFFFFFu, b1, o), p2 = __shfl_xor_sync(0xFFFFFFFFu, b2, o);
+          if (b1 >= p1) {
+            b2 = fmaxf(b2, p1);
+          } else {
+            b2 = fmaxf(p2, b1);
+            b1 = p1;
+          }
+        }
+        const float sum = a.spec.group_topn == 2 ? b1 + b2 : b1;
+        if (lane == g) my_gscore = sum;
       }
-      if (lane == g) my_gscore = sum;
+    } else {
+      for (int g = 0; g < a.spec.n_group; ++g) {
+        uint32_t taken = 0;
+        float sum = 0.f;
+        for (int r = 0; r < a.spec.group_topn; ++r) {
+          float v = -INFINITY;
+          int i = INT_MAX;
+#pragma unroll
+          for (int j = 0; j < kJMax; ++j) {
+            const int c = lane + 32 * j;
+            if (gid[j] == g && !((taken >> j) & 1u) && (sc[j] > v || (sc[j] == v && c < i))) {
+              v = sc[j];
+              i = c;
+            }
+          }
+          warp_best(v, i);
+          sum += v;
+          if (i != INT_MAX && (i & 31) == lane) taken |= 1u << (i >> 5);
+        }
+        if (lane == g) my_gscore = sum;
+      }
     }
     kept = 0;
     for (int r = 0; r < a.spec.topk_group; ++r) {
@@ -246,6 +286,9 @@ __global__ void router_topk_kernel(const TopkArgs a) {
       warp_best(v, i);
       if (i != INT_MAX) kept |= 1u << i;
     }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kJMax; ++j) gid[j] = 0;
   }
 
   // k rounds of warp arg-max over the candidate logits (the score functions
@@ -259,7 +302,7 @@ __global__ void router_topk_kernel(const TopkArgs a) {
 #pragma unroll
     for (int j = 0; j < kJMax; ++j) {
       const int c = lane + 32 * j;
-      if (c < E && ((kept >> (c / gsize)) & 1u) && !((taken >> j) & 1u)) {
+      if (c < E && ((kept >> gid[j]) & 1u) && !((taken >> j) & 1u)) {
         if (l[j] > v || (l[j] == v && c < i)) {
           v = l[j];
           i = c;

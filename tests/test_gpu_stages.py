@@ -32,6 +32,10 @@ ROUTER_CASES = [
     ("qwen2", 256, {}),
     ("skew", 256, {"alpha": 0.0}), ("skew", 512, {"alpha": 1.0}), ("skew", 512, {"alpha": 2.0}),
     ("deepseek", 512, {}),
+    # group-limited variants: 8 groups of 8 (groups inside a 32-column block),
+    # top-3 / top-1 per group, 16 groups of 16
+    ("deepseek", 256, {"E": 64}), ("deepseek", 256, {"group_topn": 3}), ("deepseek", 256, {"group_topn": 1}),
+    ("deepseek", 256, {"n_group": 16, "topk_group": 6}),
 ]
 
 
