@@ -318,6 +318,8 @@ def run_ours(args):
                       "layer_roofline_frac": tr / (ms / 1e3), "active_experts": r["active_experts"],
                       "stages_us": {k2: v * 1e3 for k2, v in r["stage_ms"].items()}})
 
+    decode = [] if (args.no_decode or args.no_sweep) else run_decode(moe, torch, d, cfg, wl_all, stream)
+
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -336,6 +338,7 @@ def run_ours(args):
         "clocks": clk,
         "gpu_launches": launches_per_forward(wl) * args.steps,
         "sweep": sweep,
+        "decode": decode,
     }
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(wl, inp, budget_s=args.cpu_seconds)
@@ -344,6 +347,73 @@ def run_ours(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+DECODE_T = (1, 2, 4, 8, 16, 32)
+
+
+def run_decode(moe, torch, d, cfg, wl_all, stream, reps=200):
+    """Decode-sized batches: the forward launched eagerly on one stream and
+    the same forward captured once in a CUDA graph and replayed.  Reports
+    device time per forward for both (CUDA events around `reps` back-to-back
+    forwards), the host time to issue one eager forward, and checks that the
+    replay writes the same bits as the eager call."""
+    res = []
+    for T in (t for t in DECODE_T if t <= d["x"].shape[0]):
+        wl = wl_all.with_T(T)
+        x = d["x"][:T]
+        out = torch.empty((T, wl.H), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(moe.moe_workspace_bytes(cfg, T, wl.H, wl.F, wl.E, wl.k), dtype=torch.uint8, device="cuda")
+
+        def fwd():
+            moe.moe_forward_ex(x, d["w_router"], d["w_gate"], d["w_up"], d["w_down"], wl.k, cfg, out=out,
+                               workspace=ws)
+
+        for _ in range(3):
+            fwd()
+        torch.cuda.synchronize()
+        ref = out.clone()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fwd()
+        b.record(stream)
+        torch.cuda.synchronize()
+        eager_us = a.elapsed_time(b) * 1e3 / reps
+        n_host = 32  # few enough that the launch queue never fills
+        t0 = time.perf_counter()
+        for _ in range(n_host):
+            fwd()
+        host_us = (time.perf_counter() - t0) * 1e6 / n_host
+        torch.cuda.synchronize()
+
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fwd()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            fwd()
+        out.zero_()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        same = bool(torch.equal(out, ref))
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        graph_us = a.elapsed_time(b) * 1e3 / reps
+        st, raw = moe.moe_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error {moe.moe_status_string(st)} {raw:#x}")
+        res.append({"T": T, "eager_us": eager_us, "graph_us": graph_us, "host_issue_us": host_us,
+                    "graph_bitwise_equal": same, "launches": launches_per_forward(wl)})
+        del g
+    return res
 
 
 def run_e2e(moe, torch, d, cfg, wl, args, stream):
@@ -472,6 +542,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the eager vs CUDA-graph decode-size timings (also skipped with --no-sweep)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:

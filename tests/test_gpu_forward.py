@@ -97,6 +97,48 @@ def test_forward_default_entry_point_matches_ex():
     assert torch.equal(a.view(torch.int16), c.view(torch.int16))  # bitwise deterministic
 
 
+@pytest.mark.parametrize("name,T", [("tiny", 64), ("qwen2", 8)])
+def test_forward_replays_in_a_cuda_graph(name, T):
+    """The forward issues no host synchronisation and no allocation with caller
+    workspace, so it can be captured once and replayed: the replay must write
+    the eager call's bits, and must follow new contents of the input buffer."""
+    wl, inp, d = _inputs(name, 2 * T, None)
+    cfg = make_cfg(wl, d)
+    x = d["x"][:T].clone()
+    out = torch.empty((T, wl.H), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(moe.moe_workspace_bytes(cfg, T, wl.H, wl.F, wl.E, wl.k), dtype=torch.uint8, device="cuda")
+
+    def fwd():
+        moe.moe_forward_ex(x, d["w_router"], d["w_gate"], d["w_up"], d["w_down"], wl.k, cfg, out=out, workspace=ws)
+
+    fwd()
+    torch.cuda.synchronize()
+    eager = out.clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fwd()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fwd()
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert moe.moe_device_error()[0] == 0
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    # new tokens in the captured input buffer
+    x.copy_(d["x"][T:2 * T])
+    g.replay()
+    torch.cuda.synchronize()
+    replayed = out.clone()
+    fwd()
+    torch.cuda.synchronize()
+    assert torch.equal(replayed.view(torch.int16), out.view(torch.int16))
+    assert not torch.equal(replayed.view(torch.int16), eager.view(torch.int16))
+
+
 def test_forward_ragged_token_counts():
     for T in (3, 127, 129, 250):
         wl, inp, d = _inputs("tiny", T, None)
