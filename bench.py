@@ -120,7 +120,8 @@ def make_cfg(moe, wl, d):
     return moe.MoeConfig.make(score=wl.score, renormalize=wl.renormalize, route_scale=wl.route_scale,
                               n_group=wl.n_group, topk_group=wl.topk_group, group_topn=wl.group_topn,
                               logit_bias=d.get("logit_bias"), ws_gate=d.get("ws_gate"), ws_up=d.get("ws_up"),
-                              ws_down=d.get("ws_down"), w_shared_gate=d.get("w_shared_gate"))
+                              ws_down=d.get("ws_down"), w_shared_gate=d.get("w_shared_gate"),
+                              activation=wl.activation)
 
 
 def launches_per_forward(wl) -> int:
@@ -159,6 +160,8 @@ def workload_overrides(args) -> dict:
     variant (groups of E / n_group experts) for small profiling captures; the
     label names the expert count, so such a line is never the headline."""
     kw = {} if args.alpha is None else {"alpha": args.alpha}
+    if args.activation is not None:
+        kw["activation"] = args.activation
     if args.experts is not None:
         base = synth.workload(args.workload)
         if args.experts < base.k or args.experts % base.n_group != 0:
@@ -537,6 +540,8 @@ def main():
     ap.add_argument("--workload", default="mixtral", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--alpha", type=float, default=None)
+    ap.add_argument("--activation", default=None, choices=["silu", "gelu"],
+                    help="gate activation of the experts (default: the workload's, SiLU)")
     ap.add_argument("--experts", type=int, default=None,
                     help="reduced expert count (same H, F, k, routing) for small profiling captures")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -57,6 +57,16 @@ typedef enum {
 typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
 
 /*
+ * Activation of the gated expert FFN, h = act(x W_gate^T) * (x W_up^T):
+ * SiLU (SwiGLU, the default) or GELU in its exact erf form (GEGLU),
+ * GELU(g) = g/2 * (1 + erf(g / sqrt(2))).  The review of "Cross-Platform
+ * Fused MoE Dispatch in Triton" names GEGLU as a dual-projection activation
+ * the same fused tile carries with only the element-wise op changed
+ * ("Editorial extensions", "Reading between the lines").
+ */
+typedef enum { MOE_ACT_SILU = 0, MOE_ACT_GELU = 1 } moe_activation_t;
+
+/*
  * Routing variant and optional shared expert.
  *  score:        softmax over all E logits, or sigmoid of each logit.
  *  renormalize:  divide the k selected scores by their sum.
@@ -89,6 +99,7 @@ typedef struct {
     const void* ws_up;
     const void* ws_down;
     const void* w_shared_gate;
+    int activation; /* moe_activation_t, for the routed and the shared experts */
 } moe_config_t;
 
 /* Fill cfg with the Mixtral routing: softmax, renormalised top-k, scale 1,
@@ -177,6 +188,13 @@ MOE_API moe_status_t moe_expert_ffn(const void* x_perm, const int32_t* offsets, 
                             int H, int F, int E,
                             const void* w_gate, const void* w_up, const void* w_down,
                             void* h, float* y, moe_stream_t stream);
+
+/* moe_expert_ffn with the activation chosen (moe_activation_t; an unknown
+ * value returns MOE_ERR_INVALID_VALUE). */
+MOE_API moe_status_t moe_expert_ffn_ex(const void* x_perm, const int32_t* offsets, int rows,
+                               int H, int F, int E,
+                               const void* w_gate, const void* w_up, const void* w_down,
+                               int activation, void* h, float* y, moe_stream_t stream);
 
 /*
  * Weighted scatter-back ("The reading": scattered back with weights).

@@ -31,8 +31,10 @@ EXPORTED_SYMBOLS = (
     "moe_config_default", "moe_route", "moe_route_scratch_bytes", "moe_permute_scratch_bytes", "moe_permute", "moe_expert_ffn",
     "moe_combine", "moe_workspace_bytes", "moe_forward_ex", "moe_forward", "moe_status_string",
     "moe_device_error", "moe_set_trace_events", "moe_selftest_wait_timeout", "moe_abi_version",
-    "moe_permute_noalloc",
+    "moe_permute_noalloc", "moe_expert_ffn_ex",
 )
+
+ACTIVATIONS = {"silu": 0, "gelu": 1}  # moe_activation_t
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_VALUE", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
           4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT", 6: "MOE_ERR_DEVICE_BOUNDS"}
@@ -59,11 +61,13 @@ class MoeConfig(ctypes.Structure):
         ("ws_up", ctypes.c_void_p),
         ("ws_down", ctypes.c_void_p),
         ("w_shared_gate", ctypes.c_void_p),
+        ("activation", ctypes.c_int),
     ]
 
     @classmethod
     def make(cls, score="softmax", renormalize=True, route_scale=1.0, n_group=1, topk_group=1, group_topn=0,
-             logit_bias=None, ws_gate=None, ws_up=None, ws_down=None, w_shared_gate=None) -> "MoeConfig":
+             logit_bias=None, ws_gate=None, ws_up=None, ws_down=None, w_shared_gate=None,
+             activation="silu") -> "MoeConfig":
         c = cls()
         c.score = {"softmax": 0, "sigmoid": 1}[score]
         c.renormalize = int(bool(renormalize))
@@ -75,6 +79,7 @@ class MoeConfig(ctypes.Structure):
         c.ws_up = _ptr(ws_up)
         c.ws_down = _ptr(ws_down)
         c.w_shared_gate = _ptr(w_shared_gate)
+        c.activation = ACTIVATIONS[activation]
         c._keep = (logit_bias, ws_gate, ws_up, ws_down, w_shared_gate)  # keep tensors alive
         return c
 
@@ -100,6 +105,7 @@ def load_library():
         "moe_permute": (I, [P, P, I, I, I, I, P, P, P, P, P, P, S, P]),
         "moe_permute_noalloc": (I, [P, P, I, I, I, I, P, P, P, P, P, P]),
         "moe_expert_ffn": (I, [P, P, I, I, I, I, P, P, P, P, P, P]),
+        "moe_expert_ffn_ex": (I, [P, P, I, I, I, I, P, P, P, I, P, P, P]),
         "moe_combine": (I, [P, P, P, P, P, I, I, I, P, P]),
         "moe_workspace_bytes": (S, [P, I, I, I, I, I]),
         "moe_forward_ex": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
@@ -232,9 +238,9 @@ def moe_permute_noalloc(topk_idx, x, E, counts=None, offsets=None, perm=None, in
     return counts, offsets, perm, inv, x_perm
 
 
-def moe_expert_ffn(x_perm, offsets, w_gate, w_up, w_down, h=None, y=None, stream=None):
-    """Grouped SwiGLU FFN.  offsets None = one dense group (w_* given as [1,...] or 2-D).
-    Returns (h bf16 [rows,F], y fp32 [rows,H])."""
+def moe_expert_ffn(x_perm, offsets, w_gate, w_up, w_down, h=None, y=None, stream=None, activation="silu"):
+    """Grouped gated FFN (SwiGLU, or GEGLU with activation="gelu").  offsets None =
+    one dense group (w_* given as [1,...] or 2-D).  Returns (h bf16 [rows,F], y fp32 [rows,H])."""
     lib = load_library()
     rows, H = x_perm.shape
     if w_gate.dim() == 2:
@@ -243,8 +249,13 @@ def moe_expert_ffn(x_perm, offsets, w_gate, w_up, w_down, h=None, y=None, stream
         E, F = w_gate.shape[0], w_gate.shape[1]
     h = _out(h, (rows, F), torch.bfloat16, x_perm.device)
     y = _out(y, (rows, H), torch.float32, x_perm.device)
-    st = lib.moe_expert_ffn(_ptr(x_perm), _ptr(offsets, torch.int32), rows, H, F, E, _ptr(w_gate), _ptr(w_up),
-                            _ptr(w_down), _ptr(h), _ptr(y, torch.float32), _stream(stream))
+    if activation == "silu":
+        st = lib.moe_expert_ffn(_ptr(x_perm), _ptr(offsets, torch.int32), rows, H, F, E, _ptr(w_gate), _ptr(w_up),
+                                _ptr(w_down), _ptr(h), _ptr(y, torch.float32), _stream(stream))
+    else:
+        st = lib.moe_expert_ffn_ex(_ptr(x_perm), _ptr(offsets, torch.int32), rows, H, F, E, _ptr(w_gate),
+                                   _ptr(w_up), _ptr(w_down), ACTIVATIONS[activation], _ptr(h),
+                                   _ptr(y, torch.float32), _stream(stream))
     _check(st, "moe_expert_ffn")
     return h, y
 

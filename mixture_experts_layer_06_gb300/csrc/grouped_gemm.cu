@@ -15,7 +15,8 @@
 // expert), tokens are B (N = bn tokens, 16..256), so a tile with few tokens
 // still runs a full-height MMA and streams weights at full width.  D^T tiles
 // live in TMEM: lane = weight row, column = token.
-//   SwiGLU:  the 128-row A tile stacks 64 gate rows over the 64 up rows of
+//   SwiGLU (or GEGLU: GELU in place of SiLU, chosen per segment):
+//            the 128-row A tile stacks 64 gate rows over the 64 up rows of
 //            the same features (one TMA box over a view in which gate and up
 //            are two planes), so ONE accumulator of bn columns holds both
 //            projections of a tile and two accumulator slots fit in TMEM:
@@ -67,6 +68,7 @@ struct SegDev {
   int groups, rows, nout, K, bn, ldo, ksplit;
   int a_mode;    // SwiGLU A loads: kStackedMap or kTwoMaps
   int up_first;  // stacked map: plane 0 is the up weights (lanes 0-63 = up)
+  int gelu;      // gated epilogue: GELU (erf form) instead of SiLU
   size_t slice_stride;
   void* out;
 };
@@ -94,6 +96,22 @@ struct Sched {
 // that the divisor stays finite (SiLU(-80) is 0 to far below bf16 resolution).
 __device__ __forceinline__ float silu(float g) {
   return __fdividef(g, 1.f + __expf(-fmaxf(g, -80.f)));
+}
+
+// GELU(g) = g/2 * (1 + erf(g / sqrt(2))), the exact form (GEGLU experts).
+__device__ __forceinline__ float gelu_erf(float g) { return 0.5f * g * (1.f + erff(g * 0.70710678118654752f)); }
+
+// h = act(g) * u for the 16 columns a warp finishes, into its bf16 staging
+// tile: own[j] are this warp's values, peer[j] its partner's.
+template <bool GELU>
+__device__ __forceinline__ void gated16(const uint32_t (&v)[32], const float (&peer)[16], int half, bool own_gate,
+                                        __nv_bfloat16* st, int lane) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float own = __uint_as_float(half ? v[16 + j] : v[j]);
+    const float gv = own_gate ? own : peer[j], uv = own_gate ? peer[j] : own;
+    st[j * 32 + lane] = __float2bfloat16_rn((GELU ? gelu_erf(gv) : silu(gv)) * uv);
+  }
 }
 
 struct GemmMaps {
@@ -468,12 +486,10 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
                 p[4 * c + 2] = f.z;
                 p[4 * c + 3] = f.w;
               }
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const float own = __uint_as_float(half ? v[16 + j] : v[j]);
-                const float gv = own_gate ? own : p[j], uv = own_gate ? p[j] : own;
-                st[j * 32 + lane] = __float2bfloat16_rn(silu(gv) * uv);
-              }
+              if (sg.gelu)
+                gated16<true>(v, p, half, own_gate, st, lane);
+              else
+                gated16<false>(v, p, half, own_gate, st, lane);
               __syncwarp();
               for (int w = lane; w < 16 * 4; w += 32) {
                 const int j = w >> 2, piece = w & 3;
@@ -705,7 +721,7 @@ cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSe
   for (int s = 0; s < num_segments; ++s) {
     const GemmSegment& g = segs[s];
     const int ks = (epi == kEpiSwiGLU || g.ksplit < 1) ? 1 : g.ksplit;
-    a.seg[s] = SegDev{g.offsets, g.groups, g.rows, g.nout, g.K, g.bn, g.ldo, ks, g.a_mode, g.up_first,
+    a.seg[s] = SegDev{g.offsets, g.groups, g.rows, g.nout, g.K, g.bn, g.ldo, ks, g.a_mode, g.up_first, g.gelu,
                       g.slice_stride, g.out};
     a.bn_max = a.bn_max > g.bn ? a.bn_max : g.bn;
     upper += static_cast<long long>(g.nout / a.munit) * ((g.rows + g.bn - 1) / g.bn + g.groups) * ks;

@@ -69,10 +69,12 @@ struct GemmSegment {
   size_t slice_stride = 0; // elements
   int a_mode = kStackedMap;  // SwiGLU only
   int up_first = 0;          // SwiGLU, kStackedMap: the view's first plane is the up weights
+  int gelu = 0;              // gated epilogue: GELU (erf form) instead of SiLU
 };
 
-// kEpiSwiGLU: gate and up rows stacked in one A tile, h = SiLU(gate) * up
-// in bf16.  kEpiStoreF32: one accumulator, fp32 out.
+// kEpiSwiGLU: gate and up rows stacked in one A tile, h = act(gate) * up in
+// bf16 (act = SiLU, or GELU with GemmSegment::gelu).  kEpiStoreF32: one
+// accumulator, fp32 out.
 enum GemmEpilogue { kEpiSwiGLU = 0, kEpiStoreF32 = 1 };
 
 // How the grouped GEMM will run these segments: as CTA pairs (tcgen05

@@ -182,6 +182,7 @@ moe_status_t check_config(const moe_config_t& c, int H, int E, int k) {
     if (!aligned16(c.ws_gate) || !aligned16(c.ws_up) || !aligned16(c.ws_down)) return MOE_ERR_INVALID_VALUE;
   }
   if (c.w_shared_gate != nullptr && !aligned16(c.w_shared_gate)) return MOE_ERR_INVALID_VALUE;
+  if (c.activation != MOE_ACT_SILU && c.activation != MOE_ACT_GELU) return MOE_ERR_INVALID_VALUE;
   (void)H;
   return MOE_OK;
 }
@@ -321,6 +322,7 @@ struct FfnOperands {
   void* h;
   float* y;
   int ksplit = 1;  // down projection K slices (y holds ksplit slices of rows*H)
+  int activation = MOE_ACT_SILU;
 };
 
 moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStream_t stream, bool traced = false) {
@@ -332,6 +334,7 @@ moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStre
     const int bn = (nseg > 1 && s == 1) ? shared_bn(o.rows, seg[0].bn) : choose_bn(o.rows, o.groups);
     seg[s] = GemmSegment{o.offsets, o.groups, o.rows, o.F, o.H, bn, o.h, o.F};
     seg[s].a_mode = stackable(o.w_gate, o.w_up) ? moe::kStackedMap : moe::kTwoMaps;
+    seg[s].gelu = o.activation == MOE_ACT_GELU ? 1 : 0;
   }
   for (int attempt = 0;; ++attempt) {
     const moe::GemmPlan plan = moe::grouped_gemm_plan(moe::kEpiSwiGLU, nseg, seg, d->num_sms);
@@ -400,9 +403,10 @@ void moe_config_default(moe_config_t* cfg) {
   cfg->n_group = 1;
   cfg->topk_group = 1;
   cfg->group_topn = 0;
+  cfg->activation = MOE_ACT_SILU;
 }
 
-int moe_abi_version(void) { return 100; }
+int moe_abi_version(void) { return 101; }
 
 moe_status_t moe_set_trace_events(void* const* events, int count) {
   if (events == nullptr || count == 0) {
@@ -487,6 +491,13 @@ moe_status_t moe_permute(const int32_t* topk_idx, const void* x, int T, int H, i
 moe_status_t moe_expert_ffn(const void* x_perm, const int32_t* offsets, int rows, int H, int F, int E,
                             const void* w_gate, const void* w_up, const void* w_down, void* h, float* y,
                             moe_stream_t stream) {
+  return moe_expert_ffn_ex(x_perm, offsets, rows, H, F, E, w_gate, w_up, w_down, MOE_ACT_SILU, h, y, stream);
+}
+
+moe_status_t moe_expert_ffn_ex(const void* x_perm, const int32_t* offsets, int rows, int H, int F, int E,
+                               const void* w_gate, const void* w_up, const void* w_down, int activation, void* h,
+                               float* y, moe_stream_t stream) {
+  if (activation != MOE_ACT_SILU && activation != MOE_ACT_GELU) return MOE_ERR_INVALID_VALUE;
   moe_status_t st = check_dims(rows, H, F, E, 1);
   if (st != MOE_OK) return st;
   if (offsets == nullptr && E != 1) return MOE_ERR_INVALID_VALUE;
@@ -498,6 +509,7 @@ moe_status_t moe_expert_ffn(const void* x_perm, const int32_t* offsets, int rows
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != MOE_OK) return st;
   FfnOperands o{x_perm, offsets, rows, E, H, F, w_gate, w_up, w_down, h, y};
+  o.activation = activation;
   return ffn_impl(d, 1, &o, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -563,13 +575,13 @@ moe_status_t moe_forward_ex(const moe_config_t* cfg, const void* x, const void* 
   const Split sp = choose_split(c, T, H, F, E, k);
   FfnOperands ops[2];
   ops[0] = FfnOperands{at(L.x_perm), offsets, Tk, E, H, F, w_gate, w_up, w_down, at(L.h_perm),
-                       static_cast<float*>(at(L.y_perm)), sp.routed};
+                       static_cast<float*>(at(L.y_perm)), sp.routed, c.activation};
   int nseg = 1;
   float* y_shared = nullptr;
   if (c.F_shared > 0) {
     y_shared = static_cast<float*>(at(L.y_shared));
     ops[1] = FfnOperands{x, nullptr, T, 1, H, c.F_shared, c.ws_gate, c.ws_up, c.ws_down, at(L.h_shared), y_shared,
-                         sp.shared};
+                         sp.shared, c.activation};
     nseg = 2;
   }
   trace(2, s);

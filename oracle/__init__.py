@@ -18,6 +18,7 @@ from .moe_oracle import (  # noqa: F401
     selection_margin,
     routing_weights,
     permute,
+    activate,
     swiglu_expert,
     combine,
     forward,

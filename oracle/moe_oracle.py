@@ -7,6 +7,9 @@ Expert Routing Without CUDA" (pith.science review page).
   variable-size GEMMs, then scattered back with weights.
 * "What carries the argument": the expert FFN is SwiGLU -- a gate and an up
   projection of the same input, SiLU(gate) * up, then the down projection.
+* "Editorial extensions" / "Reading between the lines": the same fused tile
+  carries other dual-projection activations such as GEGLU, GELU(gate) * up;
+  GELU is taken in its exact form x * Phi(x) (the page does not say which).
 * "Assumptions & free parameters": the router, top-k and SwiGLU equations are
   the standard ones of Mixtral, DeepSeek-V3 and Qwen2-MoE (Eq. (1)-(4) of the
   paper; the page names them but does not print them).  The routing variants
@@ -24,6 +27,7 @@ from __future__ import annotations
 from dataclasses import dataclass
 
 import numpy as np
+from scipy.special import erf, erfc
 
 
 def widen(a) -> np.ndarray:
@@ -165,13 +169,23 @@ def permute(idx: np.ndarray, E: int):
 
 # ----------------------------------------------------------------------------- experts
 
-def swiglu_expert(x_rows: np.ndarray, w_gate, w_up, w_down) -> np.ndarray:
-    """SwiGLU expert ("What carries the argument"):
-    y = W_down (SiLU(W_gate x) * (W_up x)),  SiLU(g) = g / (1 + exp(-g))."""
+def activate(g: np.ndarray, activation: str = "silu") -> np.ndarray:
+    """The gate activation: SiLU(g) = g / (1 + exp(-g)) (SwiGLU) or
+    GELU(g) = g / 2 * (1 + erf(g / sqrt(2))) (GEGLU, exact form)."""
+    if activation == "silu":
+        with np.errstate(over="ignore"):
+            return g / (1.0 + np.exp(-g))
+    if activation == "gelu":
+        return 0.5 * g * (1.0 + erf(g / np.sqrt(2.0)))
+    raise ValueError(activation)
+
+
+def swiglu_expert(x_rows: np.ndarray, w_gate, w_up, w_down, activation: str = "silu") -> np.ndarray:
+    """Gated expert ("What carries the argument"):
+    y = W_down (act(W_gate x) * (W_up x)), act = SiLU (SwiGLU) or GELU (GEGLU)."""
     g = x_rows @ widen(w_gate).T
     u = x_rows @ widen(w_up).T
-    with np.errstate(over="ignore"):
-        h = g / (1.0 + np.exp(-g)) * u
+    h = activate(g, activation) * u
     return h @ widen(w_down).T
 
 
@@ -183,8 +197,12 @@ def combine(Y: np.ndarray, w: np.ndarray) -> np.ndarray:
     return out
 
 
+def _act(wl) -> str:
+    return getattr(wl, "activation", "silu")
+
+
 def _shared_term(xf: np.ndarray, inp: dict, wl) -> np.ndarray:
-    ys = swiglu_expert(xf, inp["ws_gate"], inp["ws_up"], inp["ws_down"])
+    ys = swiglu_expert(xf, inp["ws_gate"], inp["ws_up"], inp["ws_down"], _act(wl))
     if wl.shared_gate:
         gate = 1.0 / (1.0 + np.exp(-(xf @ widen(inp["w_shared_gate"]))))
         ys = gate[:, None] * ys
@@ -217,7 +235,7 @@ def forward(inp: dict, wl) -> dict:
         if q.shape[0] == 0:
             continue
         t, j = q // k, q % k
-        Y[t, j] = swiglu_expert(xf[t], inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e])
+        Y[t, j] = swiglu_expert(xf[t], inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e], _act(wl))
     out = combine(Y, w)
     if wl.F_shared:
         out = out + _shared_term(xf, inp, wl)
@@ -247,7 +265,7 @@ def forward_tokens(inp: dict, wl, tokens, expert_weights=None) -> dict:
     for e in np.unique(idx):
         rows, slots = np.nonzero(idx == e)
         Y[rows, slots] = swiglu_expert(xf[rows], expert_weights("w_gate", e),
-                                       expert_weights("w_up", e), expert_weights("w_down", e))
+                                       expert_weights("w_up", e), expert_weights("w_down", e), _act(wl))
     out = combine(Y, w)
     if wl.F_shared:
         out = out + _shared_term(xf, inp, wl)
@@ -300,18 +318,24 @@ def dense_masked_forward(inp: dict, wl) -> np.ndarray:
         if routing.renormalize:
             gate[t] /= gate[t].sum()
         gate[t] *= routing.route_scale
+    gelu = _act(wl) == "gelu"
+
+    def gated(g, u):
+        # SiLU as (g u) / (1 + e^-g); GELU as (g u) * Phi(g), Phi(g) = erfc(-g / sqrt 2) / 2
+        if gelu:
+            return (g * u) * (0.5 * erfc(-g / np.sqrt(2.0)))
+        with np.errstate(over="ignore"):
+            return (g * u) / (1.0 + np.exp(-g))
+
     out = np.zeros_like(xf)
     for e in range(E):
         g = xf @ widen(inp["w_gate"][e]).T
         u = xf @ widen(inp["w_up"][e]).T
-        with np.errstate(over="ignore"):
-            h = (g * u) / (1.0 + np.exp(-g))
-        out += gate[:, e, None] * (h @ widen(inp["w_down"][e]).T)
+        out += gate[:, e, None] * (gated(g, u) @ widen(inp["w_down"][e]).T)
     if wl.F_shared:
         g = xf @ widen(inp["ws_gate"]).T
         u = xf @ widen(inp["ws_up"]).T
-        with np.errstate(over="ignore"):
-            ys = ((g * u) / (1.0 + np.exp(-g))) @ widen(inp["ws_down"]).T
+        ys = gated(g, u) @ widen(inp["ws_down"]).T
         if wl.shared_gate:
             ys = ys / (1.0 + np.exp(-(xf @ widen(inp["w_shared_gate"]))))[:, None]
         out += ys

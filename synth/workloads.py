@@ -36,6 +36,7 @@ class Workload:
     F_shared: int = 0               # 0 = no shared expert
     shared_gate: bool = False       # shared expert scaled by sigmoid(x . w_s)
     alpha: float | None = None      # Zipf skew exponent (adds a logit bias)
+    activation: str = "silu"        # gate activation: "silu" (SwiGLU) or "gelu" (GEGLU)
     seed: int = 0
 
     def with_T(self, T: int) -> "Workload":
@@ -48,6 +49,8 @@ class Workload:
             s += f" Fs={self.F_shared}"
         if self.alpha is not None:
             s += f" alpha={self.alpha:g}"
+        if self.activation != "silu":
+            s += f" act={self.activation}"
         return s
 
     # Algorithmic work of one forward over T tokens (elementwise work excluded).

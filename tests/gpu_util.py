@@ -47,7 +47,8 @@ def make_cfg(wl, d: dict) -> moe.MoeConfig:
     return moe.MoeConfig.make(score=wl.score, renormalize=wl.renormalize, route_scale=wl.route_scale,
                               n_group=wl.n_group, topk_group=wl.topk_group, group_topn=wl.group_topn,
                               logit_bias=d.get("logit_bias"), ws_gate=d.get("ws_gate"), ws_up=d.get("ws_up"),
-                              ws_down=d.get("ws_down"), w_shared_gate=d.get("w_shared_gate"))
+                              ws_down=d.get("ws_down"), w_shared_gate=d.get("w_shared_gate"),
+                              activation=wl.activation)
 
 
 def candidate_kth(scores_row: np.ndarray, wl) -> float:

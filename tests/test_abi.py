@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.moe_abi_version() == 100
+    assert lib.moe_abi_version() == 101
     assert moe.moe_status_string(0) == "MOE_OK"
     assert moe.moe_status_string(6) == "MOE_ERR_DEVICE_BOUNDS"
     assert moe.moe_status_string(99) == "MOE_ERR_UNKNOWN"
@@ -77,6 +77,9 @@ def test_null_and_misaligned_pointers_rejected(lib):
                               0x7000, 16, None) == 3  # workspace too small
     assert lib.moe_combine(None, None, None, None, None, 4, 512, 2, None, None) == 1
     assert lib.moe_expert_ffn(0x1000, None, 16, 512, 1024, 8, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, None) == 1
+    # unknown activation
+    assert lib.moe_expert_ffn_ex(0x1000, 0x7000, 16, 512, 1024, 8, 0x2000, 0x3000, 0x4000, 7, 0x5000, 0x6000,
+                                 None) == 1
 
 
 def test_bad_group_config_rejected(lib):
@@ -88,6 +91,15 @@ def test_bad_group_config_rejected(lib):
     assert lib.moe_route(ctypes.byref(c), 0x1000, 0x2000, 4, 512, 256, 8, 0x3000, 0x4000, None, 0x5000, 1 << 20, None) == 2
     c.n_group, c.topk_group, c.group_topn = 8, 1, 2  # k=8 > one group of 4 experts
     assert lib.moe_route(ctypes.byref(c), 0x1000, 0x2000, 4, 512, 32, 8, 0x3000, 0x4000, None, 0x5000, 1 << 20,
+                         None) == 1
+
+
+def test_bad_activation_rejected(lib):
+    c = moe.MoeConfig()
+    lib.moe_config_default(ctypes.byref(c))
+    assert c.activation == 0  # SiLU by default
+    c.activation = 3
+    assert lib.moe_route(ctypes.byref(c), 0x1000, 0x2000, 4, 512, 8, 2, 0x3000, 0x4000, None, 0x5000, 1 << 20,
                          None) == 1
 
 

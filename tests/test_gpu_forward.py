@@ -87,6 +87,28 @@ def test_forward_all_tokens(name, T, alpha):
         assert np.array_equal(c, orc["counts"]) and np.array_equal(p, orc["perm"])
 
 
+@pytest.mark.parametrize("name,T,kw", [("tiny", 128, {}), ("qwen2", 96, {}), ("deepseek", 256, {"E": 32})],
+                         ids=["tiny", "qwen2", "deepseek-E32"])
+def test_forward_geglu(name, T, kw):
+    """GEGLU experts (routed and shared) through the whole layer."""
+    wl = synth.workload(name, T=T, activation="gelu", **kw)
+    inp = synth.make_inputs(wl)
+    d = device_inputs(inp)
+    out, cfg = _run(wl, d)
+    if name == "deepseek":
+        tokens = _sampled_tokens(T, 24)
+        orc = oracle.forward_tokens(inp, wl, tokens)
+        gidx, gw, _ = moe.moe_route(d["x"], d["w_router"], wl.k, cfg)
+        same = check_routing(wl, gidx.cpu().numpy()[tokens], gw.cpu().numpy()[tokens], orc)
+        compare_outputs(host_f64(out)[tokens][same], orc["out"][same])
+        return
+    orc = oracle.forward(inp, wl)
+    gidx, gw, _ = moe.moe_route(d["x"], d["w_router"], wl.k, cfg)
+    same = check_routing(wl, gidx.cpu().numpy(), gw.cpu().numpy(), orc)
+    rel, mx = compare_outputs(host_f64(out)[same], orc["out"][same])
+    print(f"{wl.label}: rel-L2 {rel:.2e} max-abs {mx:.2e}")
+
+
 def test_forward_default_entry_point_matches_ex():
     wl, inp, d = _inputs("tiny", 128, None)
     a = moe.moe_forward(d["x"], d["w_router"], d["w_gate"], d["w_up"], d["w_down"], wl.k)

@@ -126,7 +126,7 @@ def _ffn_case(rows_per_group, H, F, seed=9):
     return xp, offsets, wg, wu, wd
 
 
-def _oracle_ffn(xp, offsets, wg, wu, wd):
+def _oracle_ffn(xp, offsets, wg, wu, wd, activation="silu"):
     xf = oracle.widen(xp)
     E = wg.shape[0]
     h = np.zeros((xf.shape[0], wg.shape[1]))
@@ -136,8 +136,8 @@ def _oracle_ffn(xp, offsets, wg, wu, wd):
         if b > a:
             g = xf[a:b] @ oracle.widen(wg[e]).T
             u = xf[a:b] @ oracle.widen(wu[e]).T
-            h[a:b] = g / (1 + np.exp(-g)) * u
-            y[a:b] = oracle.swiglu_expert(xf[a:b], wg[e], wu[e], wd[e])
+            h[a:b] = oracle.activate(g, activation) * u
+            y[a:b] = oracle.swiglu_expert(xf[a:b], wg[e], wu[e], wd[e], activation)
     return h, y
 
 
@@ -167,6 +167,24 @@ def test_expert_ffn(name, counts, H, F):
     rel = np.linalg.norm(y_gpu - y_or) / np.linalg.norm(y_or)
     assert rel < 4e-3, rel
     assert np.abs(y_gpu - y_or).max() <= 1e-2 * np.abs(y_or).max()
+
+
+@pytest.mark.parametrize("counts,H,F", [([5, 17, 1, 30, 0, 64], 256, 384), ([130, 100, 129, 120], 256, 640),
+                                        ([300, 257, 200, 255], 512, 512)],
+                         ids=["bn16", "bn128", "pair_tiles"])
+def test_expert_ffn_geglu(counts, H, F):
+    """GELU in place of SiLU in the same fused epilogue (GEGLU experts)."""
+    xp, offsets, wg, wu, wd = _ffn_case(counts, H, F)
+    h, y = moe.moe_expert_ffn(dev_bf16(xp), dev_i32(offsets), dev_bf16(wg), dev_bf16(wu), dev_bf16(wd),
+                              activation="gelu")
+    assert moe.moe_device_error()[0] == 0
+    h_or, y_or = _oracle_ffn(xp, offsets, wg, wu, wd, "gelu")
+    h_gpu, y_gpu = host_f64(h), host_f64(y)
+    assert np.all(np.abs(h_gpu - h_or) <= 2.0 ** -8 * np.abs(h_or) + 1e-4)
+    assert np.linalg.norm(y_gpu - y_or) / np.linalg.norm(y_or) < 4e-3
+    # and it is not the SwiGLU result
+    h_silu, _ = _oracle_ffn(xp, offsets, wg, wu, wd, "silu")
+    assert np.abs(h_gpu - h_silu).max() > 1e-2
 
 
 @pytest.mark.parametrize("counts,H,F", [([5, 17, 1, 30], 256, 384), ([300, 257, 200, 255], 512, 512)],

@@ -190,6 +190,47 @@ def _loop_swiglu(xr, wg, wu, wd):
     return [sum(wd[i][f] * h[f] for f in range(F)) for i in range(len(wd))]
 
 
+def _loop_geglu(xr, wg, wu, wd):
+    """Pure-Python GEGLU on one row: y_i = sum_f Wd[i,f] * gelu(g_f) * u_f,
+    gelu(g) = g * Phi(g) with Phi from math.erf."""
+    F, H = len(wg), len(xr)
+    h = []
+    for f in range(F):
+        g = sum(wg[f][c] * xr[c] for c in range(H))
+        u = sum(wu[f][c] * xr[c] for c in range(H))
+        h.append(g * 0.5 * (1 + math.erf(g / math.sqrt(2))) * u)
+    return [sum(wd[i][f] * h[f] for f in range(F)) for i in range(len(wd))]
+
+
+# Standard normal CDF at a few points (printed tables of the normal distribution).
+_PHI = {0.0: 0.5, 1.0: 0.8413447460685429, -1.0: 0.15865525393145707, 2.0: 0.9772498680518208,
+        -3.0: 0.0013498980316300946}
+
+
+def _gelu_table_ok(mod) -> bool:
+    x = np.array(list(_PHI))
+    want = x * np.array(list(_PHI.values()))
+    return bool(np.allclose(mod.activate(x, "gelu"), want, rtol=1e-13, atol=0.0))
+
+
+def test_gelu_matches_normal_cdf_table():
+    import oracle.moe_oracle as mo
+    assert _gelu_table_ok(mo)
+    x = np.array(list(_PHI))
+    np.testing.assert_allclose(mo.activate(x, "silu"), [v / (1 + math.exp(-v)) for v in x], rtol=1e-15)
+    with pytest.raises(ValueError):
+        mo.activate(x, "relu")
+
+
+def test_single_expert_is_plain_geglu_mlp():
+    wl, inp = _small(T=3, H=8, F=4, E=1, k=1, activation="gelu")
+    r = oracle.forward(inp, wl)
+    X = oracle.widen(inp["x"]).tolist()
+    wg, wu, wd = (oracle.widen(inp[n][0]).tolist() for n in ("w_gate", "w_up", "w_down"))
+    for t in range(3):
+        np.testing.assert_allclose(r["out"][t], _loop_geglu(X[t], wg, wu, wd), rtol=1e-12, atol=1e-14)
+
+
 def _small(T, H, F, E, k, seed=5, **kw):
     wl = Workload("small", T=T, H=H, F=F, E=E, k=k, seed=seed, **kw)
     s = seed
@@ -293,7 +334,7 @@ def test_k_equals_E_is_dense_softmax_mixture():
 
 # ----------------------------------------------------------------------------- dense
 
-@pytest.mark.parametrize("shape", ["tiny", "qwen2_like", "deepseek_like", "skew_like"])
+@pytest.mark.parametrize("shape", ["tiny", "qwen2_like", "deepseek_like", "skew_like", "geglu_deepseek_like"])
 def test_dense_masked_matches_forward(shape):
     if shape == "tiny":
         wl = synth.workload("tiny")
@@ -303,8 +344,11 @@ def test_dense_masked_matches_forward(shape):
     elif shape == "deepseek_like":
         wl, inp = _small(T=40, H=64, F=32, E=32, k=4, score="sigmoid", route_scale=2.5,
                          n_group=8, topk_group=4, group_topn=2, F_shared=32)
-    else:
+    elif shape == "skew_like":
         wl, inp = _small(T=40, H=64, F=32, E=16, k=4, alpha=2.0)
+    else:
+        wl, inp = _small(T=40, H=64, F=32, E=32, k=4, score="sigmoid", route_scale=2.5,
+                         n_group=8, topk_group=4, group_topn=2, F_shared=32, activation="gelu")
     r = oracle.forward(inp, wl)
     dense = oracle.dense_masked_forward(inp, wl)
     scale = np.abs(r["out"]).max()
@@ -360,10 +404,22 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     assert golden_ok()
     orig = mo.swiglu_expert
     monkeypatch.setattr(mo, "swiglu_expert",
-                        lambda x, g, u, d: (x @ mo.widen(g).T * (x @ mo.widen(u).T)) @ mo.widen(d).T)
+                        lambda x, g, u, d, act="silu": (x @ mo.widen(g).T * (x @ mo.widen(u).T)) @ mo.widen(d).T)
     assert not golden_ok()  # SiLU dropped
-    monkeypatch.setattr(mo, "swiglu_expert", lambda x, g, u, d: orig(x, u, g, d))
+    monkeypatch.setattr(mo, "swiglu_expert", lambda x, g, u, d, act="silu": orig(x, u, g, d, act))
     assert not golden_ok()  # gate and up swapped
     monkeypatch.setattr(mo, "swiglu_expert", orig)
+    orig_act = mo.activate
+
+    def gelu_tanh(g, act="silu"):
+        if act != "gelu":
+            return orig_act(g, act)
+        return 0.5 * g * (1 + np.tanh(np.sqrt(2 / np.pi) * (g + 0.044715 * g ** 3)))
+
+    monkeypatch.setattr(mo, "activate", gelu_tanh)
+    assert not _gelu_table_ok(mo)  # tanh approximation instead of the exact GELU
+    monkeypatch.setattr(mo, "activate", lambda g, act="silu": orig_act(g, "silu"))
+    assert not _gelu_table_ok(mo)  # activation ignored
+    monkeypatch.setattr(mo, "activate", orig_act)
     monkeypatch.setattr(mo, "_descending", lambda v: np.argsort(v, kind="stable"))
     assert not golden_ok()  # ascending selection
