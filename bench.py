@@ -322,6 +322,7 @@ def run_ours(args):
                       "stages_us": {k2: v * 1e3 for k2, v in r["stage_ms"].items()}})
 
     decode = [] if (args.no_decode or args.no_sweep) else run_decode(moe, torch, d, cfg, wl_all, stream)
+    esweep = run_expert_sweep(moe, torch, args, stream) if args.expert_sweep else None
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -343,6 +344,8 @@ def run_ours(args):
         "sweep": sweep,
         "decode": decode,
     }
+    if esweep is not None:
+        line["expert_sweep"] = esweep
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(wl, inp, budget_s=args.cpu_seconds)
     if world > 1:
@@ -353,6 +356,57 @@ def run_ours(args):
 
 
 DECODE_T = (1, 2, 4, 8, 16, 32)
+ESWEEP_T = (128, 512)
+
+
+def run_expert_sweep(moe, torch, args, stream):
+    """The expert-count sweep: E experts of width F = 8 * 14336 / E (constant
+    expert parameters), H = 4096, top-2, at the token counts of ESWEEP_T;
+    device time per forward over args.steps back-to-back forwards."""
+    from synth.workloads import EXPERT_SWEEP_E, expert_sweep
+    res = []
+    for E in EXPERT_SWEEP_E:
+        wl_all = expert_sweep(E, max(ESWEEP_T))
+        inp = synth.make_inputs(wl_all)
+        d = {}
+        for name, a in inp.items():
+            t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+            d[name] = t.cuda().view(torch.bfloat16) if a.dtype == np.uint16 else t.cuda()
+        del inp
+        cfg = make_cfg(moe, wl_all, d)
+        for T in ESWEEP_T:
+            wl = wl_all.with_T(T)
+            x = d["x"][:T]
+            out = torch.empty((T, wl.H), dtype=torch.bfloat16, device="cuda")
+            ws = torch.empty(moe.moe_workspace_bytes(cfg, T, wl.H, wl.F, wl.E, wl.k), dtype=torch.uint8,
+                             device="cuda")
+
+            def fwd():
+                moe.moe_forward_ex(x, d["w_router"], d["w_gate"], d["w_up"], d["w_down"], wl.k, cfg, out=out,
+                                   workspace=ws)
+
+            for _ in range(args.warmup):
+                fwd()
+            idx, _, _ = moe.moe_route(x, d["w_router"], wl.k, cfg)
+            active = int(torch.unique(idx).numel())
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(args.steps):
+                fwd()
+            b.record(stream)
+            torch.cuda.synchronize()
+            st, raw = moe.moe_device_error()
+            if st != 0:
+                raise RuntimeError(f"device error {moe.moe_status_string(st)} {raw:#x}")
+            us = a.elapsed_time(b) * 1e3 / args.steps
+            tr = max(wl.flops() / NOMINAL_BF16, wl.compulsory_bytes(active) / NOMINAL_HBM)
+            res.append({"workload": wl.label, "E": E, "F": wl.F, "T": T, "us_per_step": us,
+                        "tokens_per_s": T / (us / 1e6), "layer_roofline_frac": tr / (us / 1e6),
+                        "active_experts": active})
+        del d
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_decode(moe, torch, d, cfg, wl_all, stream, reps=200):
@@ -547,6 +601,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--expert-sweep", action="store_true",
+                    help="also time the expert-count sweep (E = 8..128, F = 8*14336/E, H = 4096, top-2)")
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the eager vs CUDA-graph decode-size timings (also skipped with --no-sweep)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

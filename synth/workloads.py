@@ -83,11 +83,28 @@ SKEW = Workload("skew", T=512, H=2048, F=1408, E=64, k=4, alpha=0.0)
 DEEPSEEK = Workload("deepseek", T=8192, H=7168, F=2048, E=256, k=8, score="sigmoid",
                     route_scale=2.5, n_group=8, topk_group=4, group_topn=2, F_shared=2048)
 
-WORKLOADS = {w.name: w for w in (TINY, MIXTRAL, QWEN2, SKEW, DEEPSEEK)}
+# The second Mixtral shape the review lists ("Mixtral-8x7B/22B"): the published
+# Mixtral-8x22B expert layer.
+MIXTRAL22B = Workload("mixtral22b", T=4096, H=6144, F=16384, E=8, k=2)
+
+WORKLOADS = {w.name: w for w in (TINY, MIXTRAL, QWEN2, SKEW, DEEPSEEK, MIXTRAL22B)}
 
 # Token counts each workload is run at.
 T_SWEEP = {"tiny": (128,), "mixtral": (1, 32, 128, 512, 4096), "qwen2": (128, 256, 512),
-           "skew": (128, 256, 512), "deepseek": (512, 2048, 8192)}
+           "skew": (128, 256, 512), "deepseek": (512, 2048, 8192), "mixtral22b": (1, 32, 128, 512, 4096)}
+
+# Expert-count sweep (the review's Table 5 remark: d_ffn is scaled down as the
+# expert count rises to keep total compute about constant; the target is not
+# stated).  Reading: E * F is held at the Mixtral-shaped layer's 8 * 14336, so
+# the expert parameters (and the weight bytes a small batch streams) stay
+# constant; H = 4096, top-2 softmax routing as Mixtral.
+EXPERT_SWEEP_E = (8, 16, 32, 64, 128)
+
+
+def expert_sweep(E: int, T: int) -> Workload:
+    if E not in EXPERT_SWEEP_E:
+        raise ValueError(E)
+    return Workload(f"esweep{E}", T=T, H=4096, F=8 * 14336 // E, E=E, k=2)
 SKEW_ALPHAS = (0.0, 1.0, 2.0)
 
 

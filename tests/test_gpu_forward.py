@@ -32,7 +32,7 @@ def _lib():
 
 # Largest token count each workload is run at here; smaller T use a prefix of
 # the same x (the generator indexes x by flat position) and the same weights.
-TMAX = {"tiny": 250, "mixtral": 4096, "qwen2": 512, "skew": 512, "deepseek": 8192}
+TMAX = {"tiny": 250, "mixtral": 4096, "qwen2": 512, "skew": 512, "deepseek": 8192, "mixtral22b": 4096}
 
 
 @functools.lru_cache(maxsize=1)
@@ -109,6 +109,21 @@ def test_forward_geglu(name, T, kw):
     print(f"{wl.label}: rel-L2 {rel:.2e} max-abs {mx:.2e}")
 
 
+@pytest.mark.parametrize("E,T", [(16, 96), (64, 128), (128, 200)])
+def test_forward_expert_count_sweep(E, T):
+    """The expert-count sweep's shapes: E experts of width 8 * 14336 / E."""
+    from synth.workloads import expert_sweep
+    wl = expert_sweep(E, T)
+    inp = synth.make_inputs(wl)
+    d = device_inputs(inp)
+    out, cfg = _run(wl, d)
+    orc = oracle.forward(inp, wl)
+    gidx, gw, _ = moe.moe_route(d["x"], d["w_router"], wl.k, cfg)
+    same = check_routing(wl, gidx.cpu().numpy(), gw.cpu().numpy(), orc)
+    rel, mx = compare_outputs(host_f64(out)[same], orc["out"][same])
+    print(f"{wl.label}: rel-L2 {rel:.2e} max-abs {mx:.2e}")
+
+
 def test_forward_default_entry_point_matches_ex():
     wl, inp, d = _inputs("tiny", 128, None)
     a = moe.moe_forward(d["x"], d["w_router"], d["w_gate"], d["w_up"], d["w_down"], wl.k)
@@ -172,7 +187,8 @@ def test_forward_ragged_token_counts():
 
 
 # Full-size token counts: the shapes and launch configuration the benchmark times.
-SAMPLED_CASES = [("mixtral", 4096, None, 48), ("mixtral", 512, None, 32), ("qwen2", 512, None, 32),
+SAMPLED_CASES = [("mixtral", 4096, None, 48), ("mixtral", 512, None, 32), ("mixtral22b", 4096, None, 24),
+                 ("mixtral22b", 32, None, 32), ("qwen2", 512, None, 32),
                  ("skew", 512, 2.0, 48), ("skew", 512, 0.0, 48), ("deepseek", 512, None, 24),
                  ("deepseek", 8192, None, 24)]
 
