@@ -323,6 +323,10 @@ def run_ours(args):
 
     decode = [] if (args.no_decode or args.no_sweep) else run_decode(moe, torch, d, cfg, wl_all, stream)
     esweep = run_expert_sweep(moe, torch, args, stream) if args.expert_sweep else None
+    ablation = None
+    if args.fusion_ablation:
+        ablation = run_fusion_ablation(moe, torch, d, cfg, wl_all, sorted(set([T_main] + sweep_T)), stream,
+                                       args.steps)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -346,6 +350,8 @@ def run_ours(args):
     }
     if esweep is not None:
         line["expert_sweep"] = esweep
+    if ablation is not None:
+        line["fusion_ablation"] = ablation
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(wl, inp, budget_s=args.cpu_seconds)
     if world > 1:
@@ -353,6 +359,44 @@ def run_ours(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def run_fusion_ablation(moe, torch, d, cfg, wl_all, Ts, stream, steps):
+    """The fused gate+up GEMM against the unfused form (two GEMMs with bf16
+    g, u in HBM, then the element-wise activation), on the routed experts of
+    the batch: route and permute once, then time each FFN over `steps`
+    back-to-back calls.  intermediate_bytes counts the HBM traffic of the
+    per-row intermediates (bf16): fused writes and reads h (4 rows F); unfused
+    also writes and reads g and u (12 rows F)."""
+    res = []
+    for T in Ts:
+        wl = wl_all.with_T(T)
+        x = d["x"][:T]
+        idx, _, _ = moe.moe_route(x, d["w_router"], wl.k, cfg)
+        _, offsets, _, _, x_perm = moe.moe_permute(idx, x, wl.E)
+        rows = T * wl.k
+        args = (x_perm, offsets, d["w_gate"], d["w_up"], d["w_down"])
+        out = {}
+        for name, fn in (("fused", lambda: moe.moe_expert_ffn(*args, activation=wl.activation)),
+                         ("unfused", lambda: moe.moe_expert_ffn_unfused(*args, activation=wl.activation))):
+            for _ in range(3):
+                fn()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(steps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            out[name] = a.elapsed_time(b) * 1e3 / steps
+        st, raw = moe.moe_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error {moe.moe_status_string(st)} {raw:#x}")
+        res.append({"T": T, "rows": rows, "fused_us": out["fused"], "unfused_us": out["unfused"],
+                    "unfused_over_fused": out["unfused"] / out["fused"],
+                    "intermediate_bytes": {"fused": 4 * rows * wl.F, "unfused": 12 * rows * wl.F},
+                    "scope": "routed experts: gate+up and down GEMMs (+ element-wise pass when unfused)"})
+    return res
 
 
 DECODE_T = (1, 2, 4, 8, 16, 32)
@@ -601,6 +645,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--fusion-ablation", action="store_true",
+                    help="also time the fused gate+up GEMM against two GEMMs + an element-wise pass")
     ap.add_argument("--expert-sweep", action="store_true",
                     help="also time the expert-count sweep (E = 8..128, F = 8*14336/E, H = 4096, top-2)")
     ap.add_argument("--no-decode", action="store_true",

@@ -197,6 +197,23 @@ MOE_API moe_status_t moe_expert_ffn_ex(const void* x_perm, const int32_t* offset
                                int activation, void* h, float* y, moe_stream_t stream);
 
 /*
+ * Fusion ablation, for measurement: the same grouped FFN with the gate and up
+ * projections run as two grouped GEMMs whose bf16 outputs g, u [rows, F] go
+ * to global memory, then h = act(g) * u as an element-wise pass, then the
+ * down projection ("What carries the argument": fusing gate and up removes
+ * those intermediates; the referee's minor comment 1 on the paper's section
+ * 3.3 gives the byte counts).  Arguments as moe_expert_ffn_ex plus the
+ * caller's g and u buffers (bf16 [rows, F], 16-byte aligned).  g and u are
+ * each rounded to bf16 before the activation, so h can differ from the fused
+ * result in the last bit.
+ */
+MOE_API moe_status_t moe_expert_ffn_unfused(const void* x_perm, const int32_t* offsets, int rows,
+                                    int H, int F, int E,
+                                    const void* w_gate, const void* w_up, const void* w_down,
+                                    int activation, void* g, void* u, void* h, float* y,
+                                    moe_stream_t stream);
+
+/*
  * Weighted scatter-back ("The reading": scattered back with weights).
  * out[t] = sum_{j=0..k-1} topk_w[t,j] * y_perm[inv[t*k+j]]
  *          (+ s_t * y_shared[t]), summed in fp32 in that fixed order and

@@ -17,7 +17,7 @@ import torch
 
 __all__ = [
     "MoeConfig", "MoeError", "load_library", "library_path", "moe_route", "moe_route_scratch_bytes", "moe_permute",
-    "moe_permute_scratch_bytes", "moe_permute_noalloc", "moe_expert_ffn", "moe_combine", "moe_workspace_bytes", "moe_forward_ex",
+    "moe_permute_scratch_bytes", "moe_permute_noalloc", "moe_expert_ffn", "moe_expert_ffn_unfused", "moe_combine", "moe_workspace_bytes", "moe_forward_ex",
     "moe_forward", "moe_device_error", "moe_set_trace_events", "moe_selftest_wait_timeout", "moe_status_string",
     "EXPORTED_SYMBOLS",
 ]
@@ -31,7 +31,7 @@ EXPORTED_SYMBOLS = (
     "moe_config_default", "moe_route", "moe_route_scratch_bytes", "moe_permute_scratch_bytes", "moe_permute", "moe_expert_ffn",
     "moe_combine", "moe_workspace_bytes", "moe_forward_ex", "moe_forward", "moe_status_string",
     "moe_device_error", "moe_set_trace_events", "moe_selftest_wait_timeout", "moe_abi_version",
-    "moe_permute_noalloc", "moe_expert_ffn_ex",
+    "moe_permute_noalloc", "moe_expert_ffn_ex", "moe_expert_ffn_unfused",
 )
 
 ACTIVATIONS = {"silu": 0, "gelu": 1}  # moe_activation_t
@@ -106,6 +106,7 @@ def load_library():
         "moe_permute_noalloc": (I, [P, P, I, I, I, I, P, P, P, P, P, P]),
         "moe_expert_ffn": (I, [P, P, I, I, I, I, P, P, P, P, P, P]),
         "moe_expert_ffn_ex": (I, [P, P, I, I, I, I, P, P, P, I, P, P, P]),
+        "moe_expert_ffn_unfused": (I, [P, P, I, I, I, I, P, P, P, I, P, P, P, P, P]),
         "moe_combine": (I, [P, P, P, P, P, I, I, I, P, P]),
         "moe_workspace_bytes": (S, [P, I, I, I, I, I]),
         "moe_forward_ex": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
@@ -258,6 +259,26 @@ def moe_expert_ffn(x_perm, offsets, w_gate, w_up, w_down, h=None, y=None, stream
                                    _ptr(y, torch.float32), _stream(stream))
     _check(st, "moe_expert_ffn")
     return h, y
+
+
+def moe_expert_ffn_unfused(x_perm, offsets, w_gate, w_up, w_down, activation="silu", stream=None):
+    """Fusion ablation: gate and up as two GEMMs into bf16 g, u, then the
+    element-wise activation, then the down projection.  Returns (h, y, g, u)."""
+    lib = load_library()
+    rows, H = x_perm.shape
+    if w_gate.dim() == 2:
+        E, F = 1, w_gate.shape[0]
+    else:
+        E, F = w_gate.shape[0], w_gate.shape[1]
+    g = torch.empty((rows, F), dtype=torch.bfloat16, device=x_perm.device)
+    u = torch.empty_like(g)
+    h = torch.empty_like(g)
+    y = torch.empty((rows, H), dtype=torch.float32, device=x_perm.device)
+    st = lib.moe_expert_ffn_unfused(_ptr(x_perm), _ptr(offsets, torch.int32), rows, H, F, E, _ptr(w_gate),
+                                    _ptr(w_up), _ptr(w_down), ACTIVATIONS[activation], _ptr(g), _ptr(u), _ptr(h),
+                                    _ptr(y, torch.float32), _stream(stream))
+    _check(st, "moe_expert_ffn_unfused")
+    return h, y, g, u
 
 
 def moe_combine(y_perm, inv, topk_w, y_shared=None, shared_scale=None, out=None, stream=None):

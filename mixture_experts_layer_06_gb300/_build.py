@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libmoe_gb300.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["moe_api.cu", "router.cu", "permute.cu", "grouped_gemm.cu", "combine.cu"]
+SOURCES = ["moe_api.cu", "router.cu", "permute.cu", "grouped_gemm.cu", "combine.cu", "unfused.cu"]
 HEADERS = ["ptx.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

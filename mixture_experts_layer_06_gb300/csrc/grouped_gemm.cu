@@ -503,6 +503,34 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
             }
           }
         }
+      } else if constexpr (EPI == kEpiStoreBF16) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
+        __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stg);
+        for (int u = 0; u < NSUB; ++u) {
+          const int feat0 = t.mb * a.munit + static_cast<int>(rank) * FEAT * NSUB + u * FEAT + q * 32;
+          for (int c0 = 0; c0 < ncols; c0 += 32) {
+            const int nc = min(32, ncols - c0);
+            uint32_t g[32];
+            const uint32_t ta = tmem_addr(tmem_base, q * 32, col0 + u * a.bn_max + c0);
+            if (nc == 32)
+              tmem_ld32(ta, g);
+            else
+              tmem_ld16(ta, g);
+            tmem_wait(g);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nc) st[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(g[j]));
+            __syncwarp();
+            for (int w = lane; w < nc * 4; w += 32) {
+              const int j = w >> 2, piece = w & 3;
+              const int row = t.b_row + c0 + j;
+              if (c0 + j < t.valid && row < sg.rows)
+                *reinterpret_cast<uint4*>(out + static_cast<size_t>(row) * sg.ldo + feat0 + piece * 8) =
+                    *reinterpret_cast<const uint4*>(st + j * 32 + piece * 8);
+            }
+            __syncwarp();
+          }
+        }
       } else {
         float* out = static_cast<float*>(sg.out) + t.out_off;
         float* st = reinterpret_cast<float*>(stg);
@@ -668,7 +696,7 @@ double wave_fill(GemmEpilogue epi, int num_segments, const GemmSegment* segs, in
     const long long active = g.offsets == nullptr ? 1 : (g.rows < g.groups ? g.rows : g.groups);
     if (active <= 0) continue;
     const long long per = (g.rows + active - 1) / active;
-    const int ks = (epi == kEpiSwiGLU || g.ksplit < 1) ? 1 : g.ksplit;
+    const int ks = (epi != kEpiStoreF32 || g.ksplit < 1) ? 1 : g.ksplit;
     tiles += active * ((per + g.bn - 1) / g.bn) * (g.nout / munit) * ks;
   }
   if (tiles <= 0 || units <= 0) return 1.0;
@@ -701,7 +729,7 @@ GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment
   for (int cand = 2; cand <= MOE_KPS_MAX; cand <<= 1) {
     bool ok = (227 * 1024 - fixed_smem(epi)) / (cand * per_kb) >= min_stages;
     for (int s = 0; s < num_segments && ok; ++s) {
-      const int ks = (epi == kEpiSwiGLU || segs[s].ksplit < 1) ? 1 : segs[s].ksplit;
+      const int ks = (epi != kEpiStoreF32 || segs[s].ksplit < 1) ? 1 : segs[s].ksplit;
       ok = segs[s].K % (kTileK * cand) == 0 && segs[s].K / (kTileK * cand) >= 2 * ks;
       if (epi == kEpiSwiGLU && segs[s].a_mode == kTwoMaps) ok = false;  // two 2-D boxes per stage
     }
@@ -720,7 +748,7 @@ cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSe
   long long upper = 0;
   for (int s = 0; s < num_segments; ++s) {
     const GemmSegment& g = segs[s];
-    const int ks = (epi == kEpiSwiGLU || g.ksplit < 1) ? 1 : g.ksplit;
+    const int ks = (epi != kEpiStoreF32 || g.ksplit < 1) ? 1 : g.ksplit;
     a.seg[s] = SegDev{g.offsets, g.groups, g.rows, g.nout, g.K, g.bn, g.ldo, ks, g.a_mode, g.up_first, g.gelu,
                       g.slice_stride, g.out};
     a.bn_max = a.bn_max > g.bn ? a.bn_max : g.bn;
@@ -745,6 +773,10 @@ cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSe
   if (epi == kEpiSwiGLU) {
     if (plan.nsub == 2) return launch_epi<kEpiSwiGLU, 2>(a, maps, grid, smem, plan.pair, stream);
     return launch_epi<kEpiSwiGLU, 1>(a, maps, grid, smem, plan.pair, stream);
+  }
+  if (epi == kEpiStoreBF16) {
+    if (plan.nsub == 2) return launch_epi<kEpiStoreBF16, 2>(a, maps, grid, smem, plan.pair, stream);
+    return launch_epi<kEpiStoreBF16, 1>(a, maps, grid, smem, plan.pair, stream);
   }
   if (plan.nsub == 2) return launch_epi<kEpiStoreF32, 2>(a, maps, grid, smem, plan.pair, stream);
   return launch_epi<kEpiStoreF32, 1>(a, maps, grid, smem, plan.pair, stream);

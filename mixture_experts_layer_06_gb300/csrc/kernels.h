@@ -74,8 +74,9 @@ struct GemmSegment {
 
 // kEpiSwiGLU: gate and up rows stacked in one A tile, h = act(gate) * up in
 // bf16 (act = SiLU, or GELU with GemmSegment::gelu).  kEpiStoreF32: one
-// accumulator, fp32 out.
-enum GemmEpilogue { kEpiSwiGLU = 0, kEpiStoreF32 = 1 };
+// accumulator, fp32 out (K split allowed).  kEpiStoreBF16: one accumulator,
+// bf16 out (the unfused gate / up projections of the fusion ablation).
+enum GemmEpilogue { kEpiSwiGLU = 0, kEpiStoreF32 = 1, kEpiStoreBF16 = 2 };
 
 // How the grouped GEMM will run these segments: as CTA pairs (tcgen05
 // cta_group::2; each CTA stages bn/2 token rows) or single CTAs, and with how
@@ -108,6 +109,10 @@ cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSe
 // Address of the current device's error word (nullptr if the device could
 // not be set up).
 uint32_t* device_error_word();
+
+// h = act(g) * u elementwise over n bf16 values (n a multiple of 8; the
+// unfused gated activation of the fusion ablation).
+cudaError_t launch_gated_elementwise(const void* g, const void* u, void* h, size_t n, int gelu, cudaStream_t stream);
 
 // Deterministic weighted combine.  y_perm (and y_shared) may hold nslices
 // partial-sum slices slice_stride elements apart; they are added in slice

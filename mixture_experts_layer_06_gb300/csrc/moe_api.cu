@@ -325,6 +325,8 @@ struct FfnOperands {
   int activation = MOE_ACT_SILU;
 };
 
+moe_status_t down_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStream_t stream);
+
 moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStream_t stream, bool traced = false) {
   moe::SegMaps maps[2];
   GemmSegment seg[2];
@@ -360,10 +362,19 @@ moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStre
   }
   if (moe::launch_grouped_gemm(moe::kEpiSwiGLU, nseg, seg, maps, d->num_sms, d->err, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
-  // down: B = h [rows, F], A = down weights [groups*H, F]
+  if (traced) trace(3, stream);
+  return down_impl(d, nseg, ops, stream);
+}
+
+// The down projection: B = h [rows, F], A = down weights [groups*H, F], fp32 y
+// (K-split slices when ops ask for them).
+moe_status_t down_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStream_t stream) {
+  moe::SegMaps maps[2];
+  GemmSegment seg[2];
   for (int s = 0; s < nseg; ++s) {
     const FfnOperands& o = ops[s];
-    const int bn = (nseg > 1 && s == 1) ? shared_bn(o.rows, seg[0].bn) : choose_bn(o.rows, o.groups);
+    const int bn = (nseg > 1 && s == 1) ? shared_bn(o.rows, choose_bn(ops[0].rows, ops[0].groups))
+                                        : choose_bn(o.rows, o.groups);
     seg[s] = GemmSegment{o.offsets, o.groups, o.rows, o.H, o.F, bn, o.y, o.H, o.ksplit,
                          static_cast<size_t>(o.rows) * o.H};
   }
@@ -377,10 +388,34 @@ moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStre
       return MOE_ERR_CUDA;
     maps[s].a1 = maps[s].a0;
   }
-  if (traced) trace(3, stream);
   if (moe::launch_grouped_gemm(moe::kEpiStoreF32, nseg, seg, maps, d->num_sms, d->err, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+// Fusion ablation: gate and up as two grouped GEMMs with bf16 outputs in
+// global memory, the gated activation as an element-wise pass, then the
+// same down projection.
+moe_status_t ffn_unfused_impl(DeviceState* d, const FfnOperands& o, void* g, void* u, cudaStream_t stream) {
+  GemmSegment seg = GemmSegment{o.offsets, o.groups, o.rows, o.F, o.H, choose_bn(o.rows, o.groups), g, o.F};
+  const moe::GemmPlan plan = moe::grouped_gemm_plan(moe::kEpiStoreBF16, 1, &seg, d->num_sms);
+  const uint64_t wrows = static_cast<uint64_t>(o.groups) * o.F;
+  const uint32_t brows = plan.pair ? seg.bn / 2 : seg.bn;
+  moe::SegMaps maps;
+  if (!make_gemm_map(&maps.b, o.x_rows, o.rows, o.H, brows, plan.kps)) return MOE_ERR_CUDA;
+  const void* w[2] = {o.w_gate, o.w_up};
+  void* dst[2] = {g, u};
+  for (int i = 0; i < 2; ++i) {
+    if (!make_gemm_map(&maps.a0, w[i], wrows, o.H, 128, plan.kps)) return MOE_ERR_CUDA;
+    maps.a1 = maps.a0;
+    seg.out = dst[i];
+    if (moe::launch_grouped_gemm(moe::kEpiStoreBF16, 1, &seg, &maps, d->num_sms, d->err, stream) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  if (moe::launch_gated_elementwise(g, u, o.h, static_cast<size_t>(o.rows) * o.F, o.activation == MOE_ACT_GELU,
+                                    stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return down_impl(d, 1, &o, stream);
 }
 
 }  // namespace
@@ -492,6 +527,25 @@ moe_status_t moe_expert_ffn(const void* x_perm, const int32_t* offsets, int rows
                             const void* w_gate, const void* w_up, const void* w_down, void* h, float* y,
                             moe_stream_t stream) {
   return moe_expert_ffn_ex(x_perm, offsets, rows, H, F, E, w_gate, w_up, w_down, MOE_ACT_SILU, h, y, stream);
+}
+
+moe_status_t moe_expert_ffn_unfused(const void* x_perm, const int32_t* offsets, int rows, int H, int F, int E,
+                                    const void* w_gate, const void* w_up, const void* w_down, int activation,
+                                    void* g, void* u, void* h, float* y, moe_stream_t stream) {
+  if (activation != MOE_ACT_SILU && activation != MOE_ACT_GELU) return MOE_ERR_INVALID_VALUE;
+  moe_status_t st = check_dims(rows, H, F, E, 1);
+  if (st != MOE_OK) return st;
+  if (offsets == nullptr && E != 1) return MOE_ERR_INVALID_VALUE;
+  if (rows == 0) return MOE_OK;
+  if (!x_perm || !w_gate || !w_up || !w_down || !g || !u || !h || !y) return MOE_ERR_INVALID_VALUE;
+  if (!aligned16(x_perm) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(g) ||
+      !aligned16(u) || !aligned16(h) || !aligned16(y))
+    return MOE_ERR_INVALID_VALUE;
+  DeviceState* d = nullptr;
+  if ((st = device_state(&d)) != MOE_OK) return st;
+  FfnOperands o{x_perm, offsets, rows, E, H, F, w_gate, w_up, w_down, h, y};
+  o.activation = activation;
+  return ffn_unfused_impl(d, o, g, u, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_expert_ffn_ex(const void* x_perm, const int32_t* offsets, int rows, int H, int F, int E,

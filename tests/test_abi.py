@@ -77,6 +77,8 @@ def test_null_and_misaligned_pointers_rejected(lib):
                               0x7000, 16, None) == 3  # workspace too small
     assert lib.moe_combine(None, None, None, None, None, 4, 512, 2, None, None) == 1
     assert lib.moe_expert_ffn(0x1000, None, 16, 512, 1024, 8, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, None) == 1
+    assert lib.moe_expert_ffn_unfused(0x1000, 0x7000, 16, 512, 1024, 8, 0x2000, 0x3000, 0x4000, 0, None, 0x8000,
+                                      0x5000, 0x6000, None) == 1  # no g buffer
     # unknown activation
     assert lib.moe_expert_ffn_ex(0x1000, 0x7000, 16, 512, 1024, 8, 0x2000, 0x3000, 0x4000, 7, 0x5000, 0x6000,
                                  None) == 1

@@ -227,6 +227,36 @@ def test_expert_ffn_weight_placement(counts, H, F):
     assert np.linalg.norm(y_gpu - y_or) / np.linalg.norm(y_or) < 4e-3
 
 
+@pytest.mark.parametrize("counts,H,F,act", [([5, 17, 1, 30, 0, 64], 256, 384, "silu"),
+                                            ([300, 257, 200, 255], 512, 512, "silu"),
+                                            ([130, 100, 129, 120], 256, 640, "gelu")],
+                         ids=["bn16", "pair_tiles", "bn128-gelu"])
+def test_expert_ffn_unfused_ablation(counts, H, F, act):
+    """The fusion ablation: g and u as two GEMMs with bf16 outputs, the
+    activation element-wise.  g and u are each one bf16 rounding of the
+    projections; h is act(g) * u of those rounded values, rounded once."""
+    xp, offsets, wg, wu, wd = _ffn_case(counts, H, F)
+    h, y, g, u = moe.moe_expert_ffn_unfused(dev_bf16(xp), dev_i32(offsets), dev_bf16(wg), dev_bf16(wu),
+                                            dev_bf16(wd), activation=act)
+    assert moe.moe_device_error()[0] == 0
+    xf = oracle.widen(xp)
+    g_or = np.zeros((xf.shape[0], F))
+    u_or = np.zeros_like(g_or)
+    for e in range(len(counts)):
+        a, b = offsets[e], offsets[e + 1]
+        g_or[a:b] = xf[a:b] @ oracle.widen(wg[e]).T
+        u_or[a:b] = xf[a:b] @ oracle.widen(wu[e]).T
+    g_gpu, u_gpu = host_f64(g), host_f64(u)
+    assert np.all(np.abs(g_gpu - g_or) <= 2.0 ** -8 * np.abs(g_or) + 1e-4)
+    assert np.all(np.abs(u_gpu - u_or) <= 2.0 ** -8 * np.abs(u_or) + 1e-4)
+    # h from the GPU's own rounded g, u: one more rounding
+    h_want = oracle.activate(g_gpu, act) * u_gpu
+    assert np.all(np.abs(host_f64(h) - h_want) <= 2.0 ** -8 * np.abs(h_want) + 1e-4)
+    _, y_or = _oracle_ffn(xp, offsets, wg, wu, wd, act)
+    y_gpu = host_f64(y)
+    assert np.linalg.norm(y_gpu - y_or) / np.linalg.norm(y_or) < 4e-3
+
+
 def test_dense_ffn_matches_plain_swiglu():
     xp, _, wg, wu, wd = _ffn_case([200], 512, 768)
     h, y = moe.moe_expert_ffn(dev_bf16(xp), None, dev_bf16(wg[0]), dev_bf16(wu[0]), dev_bf16(wd[0]))
