@@ -34,6 +34,8 @@ __global__ void combine_kernel(const float* __restrict__ y_perm, const int32_t* 
                                const float* __restrict__ shared_scale, int T, int H, int k,
                                __nv_bfloat16* __restrict__ out, int nslices, size_t stride, int nslices_sh,
                                size_t stride_sh) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= T) return;  // warp-uniform
   int r = -1;
@@ -78,10 +80,9 @@ cudaError_t launch_combine(const float* y_perm, const int32_t* inv, const float*
                            int nslices, size_t slice_stride, int nslices_shared, size_t slice_stride_shared) {
   const int threads = kWarpsPerBlock * 32;
   const dim3 grid((T + kWarpsPerBlock - 1) / kWarpsPerBlock, (H + 255) / 256);
-  combine_kernel<<<grid, threads, 0, stream>>>(
-      y_perm, inv, topk_w, y_shared, shared_scale, T, H, k, static_cast<__nv_bfloat16*>(out), nslices,
-      slice_stride, nslices_shared, slice_stride_shared);
-  return cudaGetLastError();
+  return launch_kernel(combine_kernel, grid, dim3(threads), 0, stream, y_perm, inv, topk_w, y_shared, shared_scale, T,
+                       H, k, static_cast<__nv_bfloat16*>(out), nslices, slice_stride, nslices_shared,
+                       slice_stride_shared);
 }
 
 }  // namespace moe

@@ -234,7 +234,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
   const int first = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int stride = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
-  if (warp == 0) build_schedule(a, *sched);
+  pdl_trigger();
   if (threadIdx.x == 64) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -247,6 +247,10 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
     for (int i = 0; i < 4; ++i) mbar_init(&xfull[i], 64);
     fence_mbar_init();
   }
+  // The offsets, the token rows and the outputs belong to earlier work of the
+  // stream.  Waiting before the TMEM allocation also means a kernel never
+  // holds TMEM while an earlier one on the same SM may still need some.
+  pdl_wait();
   if (warp == 1) {
     __syncwarp();
     if (PAIR) {
@@ -257,6 +261,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
       tmem_relinquish();
     }
   }
+  if (warp == 0) build_schedule(a, *sched);
   tc_fence_before_sync();
   __syncthreads();
   if (PAIR) cluster_sync();  // the peer's barriers exist before any remote use
@@ -613,12 +618,10 @@ cudaError_t launch_epi(const GemmArgs& a, const GemmMaps& maps, int grid, size_t
   cudaError_t e;
   if (pair) {
     if ((e = allow_big_smem(grouped_gemm_pair_kernel<EPI, NSUB>, pair_ok)) != cudaSuccess) return e;
-    grouped_gemm_pair_kernel<EPI, NSUB><<<grid, kThreads, smem, stream>>>(maps, a);
-  } else {
-    if ((e = allow_big_smem(grouped_gemm_kernel<EPI, NSUB>, single_ok)) != cudaSuccess) return e;
-    grouped_gemm_kernel<EPI, NSUB><<<grid, kThreads, smem, stream>>>(maps, a);
+    return launch_kernel(grouped_gemm_pair_kernel<EPI, NSUB>, dim3(grid), dim3(kThreads), smem, stream, maps, a);
   }
-  return cudaGetLastError();
+  if ((e = allow_big_smem(grouped_gemm_kernel<EPI, NSUB>, single_ok)) != cudaSuccess) return e;
+  return launch_kernel(grouped_gemm_kernel<EPI, NSUB>, dim3(grid), dim3(kThreads), smem, stream, maps, a);
 }
 
 uint32_t pow2_at_least(uint32_t v) {

@@ -8,6 +8,29 @@
 
 namespace moe {
 
+// Kernel launch on `stream` with programmatic dependent launch (the kernel
+// starts launching while the previous kernel of the stream finishes and
+// waits for it with pdl_wait before touching global memory).  MOE_PDL=0 at
+// build time launches with plain stream order.
+#ifndef MOE_PDL
+#define MOE_PDL 1
+#endif
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = MOE_PDL;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Routing variant as the kernels see it.
 struct RouteSpec {
   int sigmoid;       // 0 softmax, 1 sigmoid

@@ -30,6 +30,8 @@ constexpr int kWarpsPerBlock = 8;
 __global__ void bitmap_kernel(const int32_t* __restrict__ idx, int T, int E, int k, int W,
                               uint32_t* __restrict__ bitmap, uint32_t* err) {
   __shared__ uint32_t words[kWarpsPerBlock][256];
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int w = blockIdx.x * kWarpsPerBlock + warp;
   if (w >= W) return;  // warp-uniform
@@ -61,6 +63,8 @@ __global__ void __launch_bounds__(1024, 1)
                 int32_t* __restrict__ offsets, uint32_t* __restrict__ rowbase) {
   __shared__ uint32_t partial[1024];
   __shared__ int32_t off_s[257];
+  pdl_trigger();
+  pdl_wait();
   const int tid = threadIdx.x;
   const int nc = 1024 / E;  // chunks of words per expert
   const int e = tid % E, c = tid / E;
@@ -111,6 +115,8 @@ __global__ void gather_kernel(const int32_t* __restrict__ idx, const uint4* __re
                               int k, const uint32_t* __restrict__ bitmap, const uint32_t* __restrict__ rowbase,
                               int32_t* __restrict__ perm, int32_t* __restrict__ inv, uint4* __restrict__ x_perm,
                               uint32_t* err) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= T) return;  // warp-uniform
   const int rows = T * k;
@@ -154,14 +160,14 @@ cudaError_t launch_permute(const int32_t* topk_idx, const void* x, int T, int H,
   uint32_t* bitmap = static_cast<uint32_t*>(scratch);
   uint32_t* rowbase = bitmap + static_cast<size_t>(W) * E;
   const int threads = kWarpsPerBlock * 32;
-  bitmap_kernel<<<(W + kWarpsPerBlock - 1) / kWarpsPerBlock, threads, 0, stream>>>(topk_idx, T, E, k, W, bitmap,
-                                                                                 err);
-  scan_kernel<<<1, 1024, 0, stream>>>(bitmap, W, E, counts, offsets, rowbase);
+  cudaError_t e = launch_kernel(bitmap_kernel, dim3((W + kWarpsPerBlock - 1) / kWarpsPerBlock), dim3(threads), 0,
+                                stream, topk_idx, T, E, k, W, bitmap, err);
+  if (e != cudaSuccess) return e;
+  e = launch_kernel(scan_kernel, dim3(1), dim3(1024), 0, stream, bitmap, W, E, counts, offsets, rowbase);
+  if (e != cudaSuccess) return e;
   const dim3 ggrid((T + kWarpsPerBlock - 1) / kWarpsPerBlock, (H / 8 + 31) / 32);
-  gather_kernel<<<ggrid, threads, 0, stream>>>(
-      topk_idx, static_cast<const uint4*>(x), T, H / 8, E, k, bitmap, rowbase, perm, inv,
-      static_cast<uint4*>(x_perm), err);
-  return cudaGetLastError();
+  return launch_kernel(gather_kernel, ggrid, dim3(threads), 0, stream, topk_idx, static_cast<const uint4*>(x), T,
+                       H / 8, E, k, bitmap, rowbase, perm, inv, static_cast<uint4*>(x_perm), err);
 }
 
 }  // namespace moe

@@ -93,6 +93,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return mbar_wait_for(bar, parity, kWaitLimitNs, err, site);
 }
 
+// ------------------------------------------------------------------ launch overlap
+
+// Programmatic dependent launch.  pdl_trigger lets the next kernel of the
+// stream begin launching once every CTA of this grid has triggered (or
+// exited); pdl_wait blocks until the previous kernel of the stream has
+// completed and its memory is visible.  Every kernel waits before its first
+// global-memory access, so stream order is kept; only launch latency and
+// prologues (barrier setup, TMEM allocation, descriptor prefetch) overlap the
+// previous kernel's tail.  Both are no-ops for a launch without the
+// programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {

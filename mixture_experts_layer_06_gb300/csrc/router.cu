@@ -58,6 +58,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb1 = min(KB, kb0 + a.kb_per_split);
   const int nboxes = a.n_wr_boxes + (a.gate_box >= 0 ? 1 : 0);
 
+  pdl_trigger();
+  // x and the partial-logit scratch belong to earlier work of the stream;
+  // waiting before the TMEM allocation also means a kernel never holds TMEM
+  // while an earlier one on the same SM may still need some.
+  pdl_wait();
   if (threadIdx.x == 64) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -171,6 +176,8 @@ struct TopkArgs {
 };
 
 __global__ void router_topk_kernel(const TopkArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (t >= a.T) return;  // warp-uniform
   const int E = a.E;
@@ -329,6 +336,8 @@ __global__ void router_topk_kernel(const TopkArgs a) {
 // Used only when the gate vector does not fit as an extra router B row.
 __global__ void shared_gate_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ ws, int T,
                                    int H, float* __restrict__ scale) {
+  pdl_trigger();
+  pdl_wait();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= T) return;
   const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(warp) * H);
@@ -405,7 +414,9 @@ cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_wr, c
     configured[dev] = true;
   }
   const dim3 grid((T + kTileM - 1) / kTileM, p.ksplit);
-  router_gemm_kernel<<<grid, kThreads, smem, stream>>>(map_x, map_wr, p.fused_gate ? *map_ws : map_wr, g);
+  cudaError_t e = launch_kernel(router_gemm_kernel, grid, dim3(kThreads), smem, stream, map_x, map_wr,
+                                p.fused_gate ? *map_ws : map_wr, g);
+  if (e != cudaSuccess) return e;
 
   TopkArgs t{};
   t.partial = g.partial;
@@ -420,13 +431,14 @@ cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_wr, c
   t.topk_w = topk_w;
   t.shared_scale = shared_scale;
   const int warps = 8;
-  router_topk_kernel<<<(T + warps - 1) / warps, warps * 32, 0, stream>>>(t);
+  e = launch_kernel(router_topk_kernel, dim3((T + warps - 1) / warps), dim3(warps * 32), 0, stream, t);
+  if (e != cudaSuccess) return e;
   if (w_shared_gate != nullptr && shared_scale != nullptr && !p.fused_gate) {
-    shared_gate_kernel<<<(T * 32 + 255) / 256, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x),
-                                                                 static_cast<const __nv_bfloat16*>(w_shared_gate),
-                                                                 T, H, shared_scale);
+    e = launch_kernel(shared_gate_kernel, dim3((T * 32 + 255) / 256), dim3(256), 0, stream,
+                      static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_shared_gate), T, H,
+                      shared_scale);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace moe

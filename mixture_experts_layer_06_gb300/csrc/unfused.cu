@@ -10,6 +10,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -20,6 +21,8 @@ __device__ __forceinline__ float act_gelu(float g) { return 0.5f * g * (1.f + er
 // One thread per 8 consecutive values (16-byte loads and stores), grid-stride.
 __global__ void gated_elementwise_kernel(const uint4* __restrict__ g, const uint4* __restrict__ u,
                                          uint4* __restrict__ h, size_t n8, int gelu) {
+  pdl_trigger();
+  pdl_wait();
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const uint4 gv = g[i], uv = u[i];
@@ -50,9 +53,9 @@ cudaError_t launch_gated_elementwise(const void* g, const void* u, void* h, size
   size_t blocks = (n8 + threads - 1) / threads;
   const size_t cap = static_cast<size_t>(sms) * 8;  // 8 CTAs of 256 threads per SM, grid-stride beyond
   if (blocks > cap) blocks = cap;
-  gated_elementwise_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      static_cast<const uint4*>(g), static_cast<const uint4*>(u), static_cast<uint4*>(h), n8, gelu);
-  return cudaGetLastError();
+  return launch_kernel(gated_elementwise_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,
+                       static_cast<const uint4*>(g), static_cast<const uint4*>(u), static_cast<uint4*>(h), n8,
+                       gelu);
 }
 
 }  // namespace moe
