@@ -154,6 +154,23 @@ def stage_algorithmic(wl, active: int):
     return out
 
 
+def max_over_ranks(ms: float, world: int) -> float:
+    """The job's time: the slowest replica's (all-reduce MAX over the ranks of
+    the default process group; the group is gloo, so this runs on the host)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, T: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: every replica processes T tokens per step."""
+    return world * T * steps / (ms / 1e3)
+
+
 def workload_overrides(args) -> dict:
     """Per-run changes to the named layer shape: the Zipf exponent, and a
     reduced expert count (--experts) that keeps H, F, k and the routing
@@ -274,14 +291,10 @@ def run_ours(args):
         main = run_T(T_main, args.steps, args.warmup, True)
     clk = clocks.summary()
 
-    ms_main = main["ms_total"]
-    if world > 1:
-        t = torch.tensor([ms_main], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_main = float(t.item())
+    ms_main = max_over_ranks(main["ms_total"], world)
     wl = main["wl"]
     ms_step = ms_main / args.steps
-    value = world * T_main * args.steps / (ms_main / 1e3)
+    value = job_tokens_per_s(world, T_main, args.steps, ms_main)
 
     # layer roofline (nominal denominators) for this batch
     flops = wl.flops()
