@@ -34,7 +34,7 @@ def _worker(rank, world, port, local_ms, out):
 def test_max_over_ranks_and_job_throughput_two_ranks():
     world, port = 2, _free_port()
     local_ms = [40.0, 43.5]  # rank 1 is the slow replica
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.start_processes(_worker, args=(world, port, local_ms, out), nprocs=world, start_method="spawn")
         res = dict(out)
