@@ -15,20 +15,51 @@ namespace {
 
 constexpr int kWarpsPerBlock = 8;
 
+constexpr int kMaxSlices = 8;  // K slices of the down projection (at most 8)
+constexpr long long kFewWarps = 4096;  // below this many warps the grid is latency-bound
+
 // Sum of the nslices partial-sum slices of 8 consecutive fp32 values, in
-// slice order.
+// slice order.  MAXS > 0: all (<= MAXS) slices are loaded before the first
+// add, so their latencies overlap (for grids with few warps); MAXS == 0: one
+// slice after the other, in fewer registers (for grids with many warps,
+// where occupancy hides the latency).
+template <int MAXS>
 __device__ __forceinline__ void load8(const float* p, int nslices, size_t stride, float (&v)[8]) {
-  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-  for (int s = 1; s < nslices; ++s) {
-    const float4* q = reinterpret_cast<const float4*>(p + s * stride);
-    const float4 c = q[0], d = q[1];
-    v[0] += c.x; v[1] += c.y; v[2] += c.z; v[3] += c.w;
-    v[4] += d.x; v[5] += d.y; v[6] += d.z; v[7] += d.w;
+  if constexpr (MAXS == 0) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    for (int s = 1; s < nslices; ++s) {
+      const float4* q = reinterpret_cast<const float4*>(p + s * stride);
+      const float4 c = q[0], d = q[1];
+      v[0] += c.x; v[1] += c.y; v[2] += c.z; v[3] += c.w;
+      v[4] += d.x; v[5] += d.y; v[6] += d.z; v[7] += d.w;
+    }
+  } else {
+    float4 c[MAXS][2];
+#pragma unroll
+    for (int s = 0; s < MAXS; ++s) {
+      if (s < nslices) {
+        const float4* q = reinterpret_cast<const float4*>(p + s * stride);
+        c[s][0] = q[0];
+        c[s][1] = q[1];
+      }
+    }
+    v[0] = c[0][0].x; v[1] = c[0][0].y; v[2] = c[0][0].z; v[3] = c[0][0].w;
+    v[4] = c[0][1].x; v[5] = c[0][1].y; v[6] = c[0][1].z; v[7] = c[0][1].w;
+#pragma unroll
+    for (int s = 1; s < MAXS; ++s) {
+      if (s < nslices) {
+        v[0] += c[s][0].x; v[1] += c[s][0].y; v[2] += c[s][0].z; v[3] += c[s][0].w;
+        v[4] += c[s][1].x; v[5] += c[s][1].y; v[6] += c[s][1].z; v[7] += c[s][1].w;
+      }
+    }
   }
 }
 
+// MR / MS: load8's MAXS for the routed rows / the shared expert's row.  G:
+// routed rows loaded before they are added.
+template <int MR, int MS, int G>
 __global__ void combine_kernel(const float* __restrict__ y_perm, const int32_t* __restrict__ inv,
                                const float* __restrict__ topk_w, const float* __restrict__ y_shared,
                                const float* __restrict__ shared_scale, int T, int H, int k,
@@ -49,19 +80,30 @@ __global__ void combine_kernel(const float* __restrict__ y_perm, const int32_t* 
   const bool active = h0 < H;
   {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const int rj = __shfl_sync(0xFFFFFFFFu, r, j);  // all lanes take part
-      const float wj = __shfl_sync(0xFFFFFFFFu, w, j);
-      if (rj < 0 || !active) continue;
-      float v[8];
-      load8(y_perm + static_cast<size_t>(rj) * H + h0, nslices, stride, v);
+    // G expert rows are loaded before they are added (in slot order), so
+    // their memory latencies overlap.
+    for (int j0 = 0; j0 < k; j0 += G) {
+      float v[G][8], wj[G];
+      bool ok[G];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
+      for (int q = 0; q < G; ++q) {
+        const int j = j0 + q;  // lanes >= k hold r = -1
+        const int rj = __shfl_sync(0xFFFFFFFFu, r, j & 31);  // all lanes take part
+        wj[q] = __shfl_sync(0xFFFFFFFFu, w, j & 31);
+        ok[q] = j < k && rj >= 0 && active;
+        if (ok[q]) load8<MR>(y_perm + static_cast<size_t>(rj) * H + h0, nslices, stride, v[q]);
+      }
+#pragma unroll
+      for (int q = 0; q < G; ++q)
+        if (ok[q]) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[q], v[q][i], acc[i]);
+        }
     }
     if (!active) return;
     if (y_shared != nullptr) {
       float v[8];
-      load8(y_shared + static_cast<size_t>(t) * H + h0, nslices_sh, stride_sh, v);
+      load8<MS>(y_shared + static_cast<size_t>(t) * H + h0, nslices_sh, stride_sh, v);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = fmaf(s, v[i], acc[i]);
     }
@@ -78,10 +120,22 @@ __global__ void combine_kernel(const float* __restrict__ y_perm, const int32_t* 
 cudaError_t launch_combine(const float* y_perm, const int32_t* inv, const float* topk_w, const float* y_shared,
                            const float* shared_scale, int T, int H, int k, void* out, cudaStream_t stream,
                            int nslices, size_t slice_stride, int nslices_shared, size_t slice_stride_shared) {
+  if (nslices < 1 || nslices > kMaxSlices || nslices_shared < 1 || nslices_shared > kMaxSlices)
+    return cudaErrorInvalidValue;
   const int threads = kWarpsPerBlock * 32;
   const dim3 grid((T + kWarpsPerBlock - 1) / kWarpsPerBlock, (H + 255) / 256);
-  return launch_kernel(combine_kernel, grid, dim3(threads), 0, stream, y_perm, inv, topk_w, y_shared, shared_scale, T,
-                       H, k, static_cast<__nv_bfloat16*>(out), nslices, slice_stride, nslices_shared,
+  // Few warps (decode-sized batches): overlap the latencies inside each warp.
+  // Many warps: keep registers low so that occupancy hides them.
+  const long long warps = static_cast<long long>(T) * grid.y;
+  void (*kernel)(const float*, const int32_t*, const float*, const float*, const float*, int, int, int,
+                 __nv_bfloat16*, int, size_t, int, size_t) = combine_kernel<0, 0, 1>;
+  if (warps <= kFewWarps) {
+    const bool rs = nslices > 1, ss = y_shared != nullptr && nslices_shared > 1;
+    kernel = rs ? (ss ? combine_kernel<kMaxSlices, kMaxSlices, 1> : combine_kernel<kMaxSlices, 1, 1>)
+                : (ss ? combine_kernel<1, kMaxSlices, 4> : combine_kernel<1, 1, 4>);
+  }
+  return launch_kernel(kernel, grid, dim3(threads), 0, stream, y_perm, inv, topk_w, y_shared, shared_scale, T, H, k,
+                       static_cast<__nv_bfloat16*>(out), nslices, slice_stride, nslices_shared,
                        slice_stride_shared);
 }
 

@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(1024, 1)
                 int32_t* __restrict__ offsets, uint32_t* __restrict__ rowbase) {
   __shared__ uint32_t partial[1024];
   __shared__ int32_t off_s[257];
+  __shared__ int32_t warp_tot[8];
   pdl_trigger();
   pdl_wait();
   const int tid = threadIdx.x;
@@ -88,14 +89,25 @@ __global__ void __launch_bounds__(1024, 1)
     off_s[tid] = static_cast<int32_t>(run);
   }
   __syncthreads();
-  if (tid == 0) {
-    int32_t run = 0;
-    for (int ee = 0; ee < E; ++ee) {
-      const int32_t v = off_s[ee];
-      off_s[ee] = run;
-      run += v;
+  // Exclusive scan of the E <= 256 counts by the first 8 warps: shuffle scan
+  // inside each warp, then the warp totals.
+  int32_t cnt = 0, incl = 0;
+  if (tid < 256) {
+    cnt = tid < E ? off_s[tid] : 0;
+    incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if ((tid & 31) >= o) incl += n;
     }
-    off_s[E] = run;
+    if ((tid & 31) == 31) warp_tot[tid >> 5] = incl;
+  }
+  __syncthreads();
+  if (tid < 256) {
+    int32_t base = 0;
+    for (int w = 0; w < (tid >> 5); ++w) base += warp_tot[w];
+    if (tid < E) off_s[tid] = base + incl - cnt;
+    if (tid == E - 1) off_s[E] = base + incl;
   }
   __syncthreads();
   for (int ee = tid; ee <= E; ee += 1024) offsets[ee] = off_s[ee];
