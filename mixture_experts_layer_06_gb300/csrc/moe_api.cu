@@ -215,13 +215,17 @@ size_t route_scratch(const moe_config_t& c, int T, int H, int E) {
 
 // K-split of the down projection in moe_forward_ex.  When the routed rows
 // give too few output tiles to fill the GPU several times over (small T:
-// few active experts and one token tile each), K (= F) is cut into
-// 2, 4 or 8 slices whose fp32 partial sums go to separate y slices; the
-// combine adds them in slice order, so the result stays deterministic.  The
-// shared expert's K (= F_shared) is cut so that its slices are no longer
-// than the routed ones.  Depends only on the shapes (not on the device), so
-// that moe_workspace_bytes() can size the slices.
+// few active experts and one token tile each), K (= F) is cut into S <= 8
+// slices whose fp32 partial sums go to separate y slices; the combine adds
+// them in slice order, so the result stays deterministic.  S minimises a
+// two-term estimate: the weight bytes times the wave-quantisation loss of
+// tiles * S tiles on 152 SMs, plus the partial sums written and read back
+// (2 * S * T k * H * 4 bytes); a slice keeps >= 8 K blocks.  The shared
+// expert's K (= F_shared) is cut so that its slices are no longer than the
+// routed ones.  Depends only on the shapes (not on the device), so that
+// moe_workspace_bytes() can size the slices.
 constexpr long long kTargetTiles = 6 * 152;
+constexpr int kSms = 152;
 
 struct Split {
   int routed = 1, shared = 1;
@@ -236,7 +240,19 @@ Split choose_split(const moe_config_t& c, int T, int H, int F, int E, int k) {
   const int bn = choose_bn(Tk, E);
   const long long tiles = groups * (H / 128) * ((rows_per + bn - 1) / bn);
   const int kb = F / 64;
-  while (sp.routed < 8 && tiles * sp.routed < kTargetTiles && kb / (2 * sp.routed) >= 8) sp.routed <<= 1;
+  if (tiles < kTargetTiles) {
+    const double weights = 2.0 * groups * H * F;
+    double best = 0.0;
+    for (int S = 1; S <= 8 && kb / S >= 8; ++S) {
+      const long long n = tiles * S;
+      const double wave_loss = static_cast<double>((n + kSms - 1) / kSms * kSms) / static_cast<double>(n);
+      const double cost = weights * wave_loss + 2.0 * S * Tk * H * 4.0;
+      if (S == 1 || cost < best * 0.99) {  // a larger S must win by more than 1 %
+        best = cost;
+        sp.routed = S;
+      }
+    }
+  }
   if (c.F_shared > 0) {
     const long long slice = F / sp.routed;
     const int kbs = c.F_shared / 64;
