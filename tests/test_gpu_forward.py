@@ -17,6 +17,7 @@ import torch
 import mixture_experts_layer_06_gb300 as moe
 import oracle
 import synth
+from synth.workloads import Workload
 
 from gpu_util import (check_grouping, check_routing, compare_outputs, device_inputs, host_f64, make_cfg)
 
@@ -122,6 +123,24 @@ def test_forward_expert_count_sweep(E, T):
     same = check_routing(wl, gidx.cpu().numpy(), gw.cpu().numpy(), orc)
     rel, mx = compare_outputs(host_f64(out)[same], orc["out"][same])
     print(f"{wl.label}: rel-L2 {rel:.2e} max-abs {mx:.2e}")
+
+
+@pytest.mark.parametrize("shape", ["k16_of_32", "one_expert", "k_equals_E"])
+def test_forward_limits_and_degenerate_routing(shape):
+    """The largest top-k the kernels take (16), a layer with a single expert
+    (every token's one weight is 1), and k = E (every expert on every token)."""
+    kw = {"k16_of_32": dict(E=32, k=16), "one_expert": dict(E=1, k=1), "k_equals_E": dict(E=8, k=8)}[shape]
+    wl = Workload(shape, T=77, H=256, F=384, **kw)
+    inp = synth.make_inputs(wl)
+    d = device_inputs(inp)
+    out, cfg = _run(wl, d)
+    orc = oracle.forward(inp, wl)
+    gidx, gw, _ = moe.moe_route(d["x"], d["w_router"], wl.k, cfg)
+    same = check_routing(wl, gidx.cpu().numpy(), gw.cpu().numpy(), orc)
+    compare_outputs(host_f64(out)[same], orc["out"][same])
+    if wl.k == wl.E:  # every token picks every expert: the grouping is the identity per expert
+        counts, _, _, _, _ = moe.moe_permute(gidx, d["x"], wl.E)
+        assert np.all(counts.cpu().numpy() == wl.T)
 
 
 def test_forward_default_entry_point_matches_ex():
