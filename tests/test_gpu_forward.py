@@ -125,6 +125,30 @@ def test_forward_expert_count_sweep(E, T):
     print(f"{wl.label}: rel-L2 {rel:.2e} max-abs {mx:.2e}")
 
 
+@functools.lru_cache(maxsize=1)
+def _deepseek32():
+    wl = synth.workload("deepseek", T=40, E=32)
+    inp = synth.make_inputs(wl)
+    return wl, inp, device_inputs(inp)
+
+
+@pytest.mark.parametrize("T", [1, 3, 40])
+def test_forward_deepseek_shape_decode_sizes(T):
+    """DeepSeek-V3-shaped experts (32 of them, same H, F, k, group routing and
+    shared expert) at decode-sized batches: K-split down projection, the
+    few-warp combine, one-row tiles.  Smaller T use a prefix of the same x."""
+    wl_full, inp_full, d_full = _deepseek32()
+    wl = wl_full.with_T(T)
+    inp, d = dict(inp_full), dict(d_full)
+    inp["x"], d["x"] = inp_full["x"][:T], d_full["x"][:T]
+    out, cfg = _run(wl, d)
+    orc = oracle.forward(inp, wl)
+    gidx, gw, _ = moe.moe_route(d["x"], d["w_router"], wl.k, cfg)
+    same = check_routing(wl, gidx.cpu().numpy(), gw.cpu().numpy(), orc)
+    rel, mx = compare_outputs(host_f64(out)[same], orc["out"][same])
+    print(f"{wl.label}: rel-L2 {rel:.2e} max-abs {mx:.2e}")
+
+
 @pytest.mark.parametrize("shape", ["k16_of_32", "one_expert", "k_equals_E"])
 def test_forward_limits_and_degenerate_routing(shape):
     """The largest top-k the kernels take (16), a layer with a single expert
