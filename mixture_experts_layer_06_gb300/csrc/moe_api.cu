@@ -692,6 +692,11 @@ moe_status_t moe_forward(const void* x, const void* w_router, const void* w_gate
   moe_status_t st = check_dims(T, H, F, E, k);
   if (st != MOE_OK) return st;
   if (T == 0) return MOE_OK;
+  // the pointer checks of moe_forward_ex, before the workspace is grown
+  if (!x || !w_router || !w_gate || !w_up || !w_down || !out) return MOE_ERR_INVALID_VALUE;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+      !aligned16(out))
+    return MOE_ERR_INVALID_VALUE;
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != MOE_OK) return st;
   const size_t need = layout(c, T, H, F, E, k).total;
