@@ -360,6 +360,10 @@ def run_ours(args):
 
     decode = [] if (args.no_decode or args.no_sweep) else run_decode(moe, torch, d, cfg, wl_all, stream)
     esweep = run_expert_sweep(moe, torch, args, stream) if args.expert_sweep else None
+    sched = None
+    if args.schedule_ablation:
+        sched = run_schedule_ablation(moe, torch, d, cfg, wl_all, sorted(set([T_main] + sweep_T)), stream,
+                                      args.steps)
     ablation = None
     if args.fusion_ablation:
         ablation = run_fusion_ablation(moe, torch, d, cfg, wl_all, sorted(set([T_main] + sweep_T)), stream,
@@ -389,6 +393,8 @@ def run_ours(args):
         line["expert_sweep"] = esweep
     if ablation is not None:
         line["fusion_ablation"] = ablation
+    if sched is not None:
+        line["schedule_ablation"] = sched
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(wl, inp, budget_s=args.cpu_seconds)
     if world > 1:
@@ -433,6 +439,40 @@ def run_fusion_ablation(moe, torch, d, cfg, wl_all, Ts, stream, steps):
                     "unfused_over_fused": out["unfused"] / out["fused"],
                     "intermediate_bytes": {"fused": 4 * rows * wl.F, "unfused": 12 * rows * wl.F},
                     "scope": "routed experts: gate+up and down GEMMs (+ element-wise pass when unfused)"})
+    return res
+
+
+def run_schedule_ablation(moe, torch, d, cfg, wl_all, Ts, stream, steps, block_m=64):
+    """The persistent, device-scheduled grouped FFN against the pages'
+    schedule (expert counts read back to the host with a synchronisation,
+    fixed block_m token tiles, one CTA per tile), on the routed experts of the
+    batch; each timed over `steps` back-to-back calls."""
+    res = []
+    for T in Ts:
+        wl = wl_all.with_T(T)
+        x = d["x"][:T]
+        idx, _, _ = moe.moe_route(x, d["w_router"], wl.k, cfg)
+        counts, offsets, _, _, x_perm = moe.moe_permute(idx, x, wl.E)
+        args = (x_perm, offsets, d["w_gate"], d["w_up"], d["w_down"])
+        out = {}
+        for name, fn in (("persistent", lambda: moe.moe_expert_ffn(*args)),
+                         ("static", lambda: moe.moe_expert_ffn_static(*args, block_m=block_m))):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()  # wall clock: the static schedule synchronises with the host
+            for _ in range(steps):
+                fn()
+            torch.cuda.synchronize()
+            out[name] = (time.perf_counter() - t0) * 1e6 / steps
+        st, raw = moe.moe_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error {moe.moe_status_string(st)} {raw:#x}")
+        c = counts.cpu()
+        res.append({"T": T, "persistent_us": out["persistent"], "static_us": out["static"],
+                    "static_over_persistent": out["static"] / out["persistent"], "block_m": block_m,
+                    "active_experts": int((c > 0).sum()), "max_rows_per_expert": int(c.max()),
+                    "timing": "host wall clock per call, back-to-back, both arms"})
     return res
 
 
@@ -682,6 +722,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--schedule-ablation", action="store_true",
+                    help="also time the persistent device schedule against host-read counts, fixed 64-row "
+                         "tiles and one CTA per tile")
     ap.add_argument("--fusion-ablation", action="store_true",
                     help="also time the fused gate+up GEMM against two GEMMs + an element-wise pass")
     ap.add_argument("--expert-sweep", action="store_true",

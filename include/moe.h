@@ -214,6 +214,24 @@ MOE_API moe_status_t moe_expert_ffn_unfused(const void* x_perm, const int32_t* o
                                     moe_stream_t stream);
 
 /*
+ * Schedule ablation, for measurement: the grouped SwiGLU FFN (as
+ * moe_expert_ffn) run the way the pages' design schedules it ("Load-bearing
+ * premise": a compile-time fixed tile size and a static expert-to-block
+ * schedule; the referee's minor comment 5 on its host-device sync).  The
+ * expert offsets are copied back to the host and the call WAITS for them
+ * (cudaStreamSynchronize on `stream`), every tile has block_m token rows
+ * (16, 32, 64, 128 or 256; an expert's rows are split into equal tiles of at
+ * most block_m rows), and each GEMM is launched with one CTA per tile (no
+ * persistent CTAs, no CTA pairs, one 128-row weight tile per CTA).  offsets
+ * must not be NULL.  The results equal moe_expert_ffn's bit for bit.  Not
+ * capturable in a CUDA graph.
+ */
+MOE_API moe_status_t moe_expert_ffn_static(const void* x_perm, const int32_t* offsets, int rows,
+                                   int H, int F, int E,
+                                   const void* w_gate, const void* w_up, const void* w_down,
+                                   int block_m, void* h, float* y, moe_stream_t stream);
+
+/*
  * Weighted scatter-back ("The reading": scattered back with weights).
  * out[t] = sum_{j=0..k-1} topk_w[t,j] * y_perm[inv[t*k+j]]
  *          (+ s_t * y_shared[t]), summed in fp32 in that fixed order and

@@ -17,7 +17,8 @@ import torch
 
 __all__ = [
     "MoeConfig", "MoeError", "load_library", "library_path", "moe_route", "moe_route_scratch_bytes", "moe_permute",
-    "moe_permute_scratch_bytes", "moe_permute_noalloc", "moe_expert_ffn", "moe_expert_ffn_unfused", "moe_combine", "moe_workspace_bytes", "moe_forward_ex",
+    "moe_permute_scratch_bytes", "moe_permute_noalloc", "moe_expert_ffn", "moe_expert_ffn_unfused",
+    "moe_expert_ffn_static", "moe_combine", "moe_workspace_bytes", "moe_forward_ex",
     "moe_forward", "moe_device_error", "moe_set_trace_events", "moe_selftest_wait_timeout", "moe_status_string",
     "EXPORTED_SYMBOLS",
 ]
@@ -31,7 +32,7 @@ EXPORTED_SYMBOLS = (
     "moe_config_default", "moe_route", "moe_route_scratch_bytes", "moe_permute_scratch_bytes", "moe_permute", "moe_expert_ffn",
     "moe_combine", "moe_workspace_bytes", "moe_forward_ex", "moe_forward", "moe_status_string",
     "moe_device_error", "moe_set_trace_events", "moe_selftest_wait_timeout", "moe_abi_version",
-    "moe_permute_noalloc", "moe_expert_ffn_ex", "moe_expert_ffn_unfused",
+    "moe_permute_noalloc", "moe_expert_ffn_ex", "moe_expert_ffn_unfused", "moe_expert_ffn_static",
 )
 
 ACTIVATIONS = {"silu": 0, "gelu": 1}  # moe_activation_t
@@ -107,6 +108,7 @@ def load_library():
         "moe_expert_ffn": (I, [P, P, I, I, I, I, P, P, P, P, P, P]),
         "moe_expert_ffn_ex": (I, [P, P, I, I, I, I, P, P, P, I, P, P, P]),
         "moe_expert_ffn_unfused": (I, [P, P, I, I, I, I, P, P, P, I, P, P, P, P, P]),
+        "moe_expert_ffn_static": (I, [P, P, I, I, I, I, P, P, P, I, P, P, P]),
         "moe_combine": (I, [P, P, P, P, P, I, I, I, P, P]),
         "moe_workspace_bytes": (S, [P, I, I, I, I, I]),
         "moe_forward_ex": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, S, P]),
@@ -279,6 +281,21 @@ def moe_expert_ffn_unfused(x_perm, offsets, w_gate, w_up, w_down, activation="si
                                     _ptr(y, torch.float32), _stream(stream))
     _check(st, "moe_expert_ffn_unfused")
     return h, y, g, u
+
+
+def moe_expert_ffn_static(x_perm, offsets, w_gate, w_up, w_down, block_m=64, stream=None):
+    """Schedule ablation: offsets read back to the host (a sync), fixed block_m
+    token tiles, one CTA per tile.  Returns (h bf16 [rows,F], y fp32 [rows,H])."""
+    lib = load_library()
+    rows, H = x_perm.shape
+    E, F = w_gate.shape[0], w_gate.shape[1]
+    h = torch.empty((rows, F), dtype=torch.bfloat16, device=x_perm.device)
+    y = torch.empty((rows, H), dtype=torch.float32, device=x_perm.device)
+    st = lib.moe_expert_ffn_static(_ptr(x_perm), _ptr(offsets, torch.int32), rows, H, F, E, _ptr(w_gate),
+                                   _ptr(w_up), _ptr(w_down), int(block_m), _ptr(h), _ptr(y, torch.float32),
+                                   _stream(stream))
+    _check(st, "moe_expert_ffn_static")
+    return h, y
 
 
 def moe_combine(y_perm, inv, topk_w, y_shared=None, shared_scale=None, out=None, stream=None):

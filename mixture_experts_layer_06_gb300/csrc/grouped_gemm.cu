@@ -709,15 +709,16 @@ double wave_fill(GemmEpilogue epi, int num_segments, const GemmSegment* segs, in
 
 }  // namespace
 
-GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment* segs, int num_sms) {
+GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment* segs, int num_sms,
+                           bool static_grid) {
   GemmPlan p{};
   const int bn_max = bn_max_of(num_segments, segs);
   const int feat = feat_per_cta(epi);
-  p.nsub = gemm_nsub(bn_max);
+  p.nsub = static_grid ? 1 : gemm_nsub(bn_max);
   for (int s = 0; s < num_segments; ++s)
     while (p.nsub > 1 && segs[s].nout % (p.nsub * feat) != 0) p.nsub >>= 1;
   const int pair_min = epi == kEpiSwiGLU ? MOE_PAIR_MIN_BN_SWIGLU : MOE_PAIR_MIN_BN;
-  p.pair = pair_min > 0 && bn_max >= pair_min;
+  p.pair = !static_grid && pair_min > 0 && bn_max >= pair_min;
   for (int s = 0; s < num_segments; ++s) p.pair = p.pair && segs[s].nout % (2 * p.nsub * feat) == 0;
   if (p.nsub > 1 && !p.pair) {
     const double fill = wave_fill(epi, num_segments, segs, feat * p.nsub, num_sms);
@@ -742,8 +743,8 @@ GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment
 }
 
 cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSegment* segs, const SegMaps* seg_maps,
-                                int num_sms, uint32_t* err, cudaStream_t stream) {
-  const GemmPlan plan = grouped_gemm_plan(epi, num_segments, segs, num_sms);
+                                int num_sms, uint32_t* err, cudaStream_t stream, long long static_ctas) {
+  const GemmPlan plan = grouped_gemm_plan(epi, num_segments, segs, num_sms, static_ctas > 0);
   GemmArgs a{};
   a.nseg = num_segments;
   a.err = err;
@@ -768,6 +769,7 @@ cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSe
   const size_t smem = static_cast<size_t>(fixed_smem(epi)) + static_cast<size_t>(stages) * stage_bytes;
   int units = plan.pair ? num_sms / 2 : num_sms;  // CTAs, or CTA pairs
   if (upper < units) units = static_cast<int>(upper);
+  if (static_ctas > 0) units = static_cast<int>(static_ctas < (1ll << 30) ? static_ctas : (1ll << 30));
   if (units < 1) units = 1;
   const int grid = plan.pair ? 2 * units : units;
   GemmMaps maps;

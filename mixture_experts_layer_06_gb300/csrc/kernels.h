@@ -110,7 +110,10 @@ struct GemmPlan {
   int kps;
   int nsub;  // sub-tiles per CTA and tile (1 or 2; see gemm_nsub)
 };
-GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment* segs, int num_sms);
+// static_grid: the schedule ablation's plan (one 128-row weight tile per CTA,
+// no CTA pairs), for launches with one CTA per tile.
+GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment* segs, int num_sms,
+                           bool static_grid = false);
 
 // TMA descriptors of one grouped-GEMM segment; b covers the [rows, K] token
 // rows with box {64 columns, bn (or bn/2) rows}, as a 3-D view {64, rows,
@@ -126,8 +129,12 @@ struct SegMaps {
 };
 
 // Persistent grouped GEMM over one or two segments (seg_maps[s] for segment s).
+// static_ctas > 0: the schedule ablation instead -- a grid of static_ctas
+// CTAs (the tile count, known on the host), each running at most one tile,
+// with the static_grid plan.
 cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSegment* segs,
-                                const SegMaps* seg_maps, int num_sms, uint32_t* err, cudaStream_t stream);
+                                const SegMaps* seg_maps, int num_sms, uint32_t* err, cudaStream_t stream,
+                                long long static_ctas = 0);
 
 // Address of the current device's error word (nullptr if the device could
 // not be set up).

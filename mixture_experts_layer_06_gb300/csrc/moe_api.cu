@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/moe.h"
 #include "kernels.h"
@@ -455,6 +456,61 @@ moe_status_t ffn_unfused_impl(DeviceState* d, const FfnOperands& o, void* g, voi
   return down_impl(d, 1, &o, stream);
 }
 
+// Schedule ablation: the expert counts are read back to the host (a
+// synchronisation), the token tile is a fixed block_m, and each grouped GEMM
+// is launched with one CTA per tile, one 128-row weight tile per CTA.
+moe_status_t ffn_static_impl(DeviceState* d, const FfnOperands& o, int block_m, cudaStream_t stream) {
+  std::vector<int32_t> off(static_cast<size_t>(o.groups) + 1);
+  if (cudaMemcpyAsync(off.data(), o.offsets, off.size() * sizeof(int32_t), cudaMemcpyDeviceToHost, stream) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  long long token_tiles = 0;
+  for (int g = 0; g < o.groups; ++g) {
+    const long long r = static_cast<long long>(off[g + 1]) - off[g];
+    if (r < 0 || off[g + 1] > o.rows) return MOE_ERR_INVALID_VALUE;
+    token_tiles += (r + block_m - 1) / block_m;
+  }
+  if (token_tiles == 0) return MOE_OK;
+  // gate+up: 64 features per CTA (one stacked gate/up tile)
+  GemmSegment seg = GemmSegment{o.offsets, o.groups, o.rows, o.F, o.H, block_m, o.h, o.F};
+  seg.a_mode = stackable(o.w_gate, o.w_up) ? moe::kStackedMap : moe::kTwoMaps;
+  seg.gelu = o.activation == MOE_ACT_GELU ? 1 : 0;
+  moe::SegMaps maps;
+  for (int attempt = 0;; ++attempt) {
+    const moe::GemmPlan plan = moe::grouped_gemm_plan(moe::kEpiSwiGLU, 1, &seg, d->num_sms, true);
+    const uint64_t wrows = static_cast<uint64_t>(o.groups) * o.F;
+    if (seg.a_mode == moe::kStackedMap) {
+      if (!make_stacked_map(&maps.a0, o.w_gate, o.w_up, wrows, o.H, plan.kps, &seg.up_first)) {
+        if (attempt > 0) return MOE_ERR_CUDA;
+        seg.a_mode = moe::kTwoMaps;
+        continue;
+      }
+      maps.a1 = maps.a0;
+    } else if (!make_map(&maps.a0, o.w_gate, wrows, o.H, 64) || !make_map(&maps.a1, o.w_up, wrows, o.H, 64)) {
+      return MOE_ERR_CUDA;
+    }
+    if (!make_gemm_map(&maps.b, o.x_rows, o.rows, o.H, block_m, plan.kps)) return MOE_ERR_CUDA;
+    break;
+  }
+  if (moe::launch_grouped_gemm(moe::kEpiSwiGLU, 1, &seg, &maps, d->num_sms, d->err, stream,
+                               token_tiles * (o.F / 64)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  // down: 128 output rows per CTA
+  GemmSegment dseg = GemmSegment{o.offsets, o.groups, o.rows, o.H, o.F, block_m, o.y, o.H, 1,
+                                 static_cast<size_t>(o.rows) * o.H};
+  const moe::GemmPlan dplan = moe::grouped_gemm_plan(moe::kEpiStoreF32, 1, &dseg, d->num_sms, true);
+  moe::SegMaps dmaps;
+  if (!make_gemm_map(&dmaps.a0, o.w_down, static_cast<uint64_t>(o.groups) * o.H, o.F, 128, dplan.kps) ||
+      !make_gemm_map(&dmaps.b, o.h, o.rows, o.F, block_m, dplan.kps))
+    return MOE_ERR_CUDA;
+  dmaps.a1 = dmaps.a0;
+  if (moe::launch_grouped_gemm(moe::kEpiStoreF32, 1, &dseg, &dmaps, d->num_sms, d->err, stream,
+                               token_tiles * (o.H / 128)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 }  // namespace
 
 namespace moe {
@@ -564,6 +620,24 @@ moe_status_t moe_expert_ffn(const void* x_perm, const int32_t* offsets, int rows
                             const void* w_gate, const void* w_up, const void* w_down, void* h, float* y,
                             moe_stream_t stream) {
   return moe_expert_ffn_ex(x_perm, offsets, rows, H, F, E, w_gate, w_up, w_down, MOE_ACT_SILU, h, y, stream);
+}
+
+moe_status_t moe_expert_ffn_static(const void* x_perm, const int32_t* offsets, int rows, int H, int F, int E,
+                                   const void* w_gate, const void* w_up, const void* w_down, int block_m, void* h,
+                                   float* y, moe_stream_t stream) {
+  if (block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128 && block_m != 256)
+    return MOE_ERR_INVALID_VALUE;
+  moe_status_t st = check_dims(rows, H, F, E, 1);
+  if (st != MOE_OK) return st;
+  if (rows == 0) return MOE_OK;
+  if (!x_perm || !offsets || !w_gate || !w_up || !w_down || !h || !y) return MOE_ERR_INVALID_VALUE;
+  if (!aligned16(x_perm) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(h) ||
+      !aligned16(y))
+    return MOE_ERR_INVALID_VALUE;
+  DeviceState* d = nullptr;
+  if ((st = device_state(&d)) != MOE_OK) return st;
+  FfnOperands o{x_perm, offsets, rows, E, H, F, w_gate, w_up, w_down, h, y};
+  return ffn_static_impl(d, o, block_m, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_expert_ffn_unfused(const void* x_perm, const int32_t* offsets, int rows, int H, int F, int E,

@@ -79,6 +79,10 @@ def test_null_and_misaligned_pointers_rejected(lib):
     assert lib.moe_expert_ffn(0x1000, None, 16, 512, 1024, 8, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, None) == 1
     assert lib.moe_expert_ffn_unfused(0x1000, 0x7000, 16, 512, 1024, 8, 0x2000, 0x3000, 0x4000, 0, None, 0x8000,
                                       0x5000, 0x6000, None) == 1  # no g buffer
+    assert lib.moe_expert_ffn_static(0x1000, 0x7000, 16, 512, 1024, 8, 0x2000, 0x3000, 0x4000, 48, 0x5000, 0x6000,
+                                     None) == 1  # block_m not a supported tile
+    assert lib.moe_expert_ffn_static(0x1000, None, 16, 512, 1024, 8, 0x2000, 0x3000, 0x4000, 64, 0x5000, 0x6000,
+                                     None) == 1  # offsets required
     # unknown activation
     assert lib.moe_expert_ffn_ex(0x1000, 0x7000, 16, 512, 1024, 8, 0x2000, 0x3000, 0x4000, 7, 0x5000, 0x6000,
                                  None) == 1

@@ -257,6 +257,25 @@ def test_expert_ffn_unfused_ablation(counts, H, F, act):
     assert np.linalg.norm(y_gpu - y_or) / np.linalg.norm(y_or) < 4e-3
 
 
+@pytest.mark.parametrize("counts,H,F,block_m", [([5, 17, 1, 30, 0, 64], 256, 384, 16),
+                                                ([130, 100, 129, 120, 300, 1], 256, 640, 64),
+                                                ([300, 257, 200, 255], 512, 512, 128)],
+                         ids=["bm16", "bm64", "bm128"])
+def test_expert_ffn_static_schedule_ablation(counts, H, F, block_m):
+    """The pages' schedule (host-read counts, fixed tiles, one CTA per tile)
+    computes the same dot products in the same order: bit-equal to the
+    persistent kernel's result."""
+    xp, offsets, wg, wu, wd = _ffn_case(counts, H, F)
+    args = (dev_bf16(xp), dev_i32(offsets), dev_bf16(wg), dev_bf16(wu), dev_bf16(wd))
+    h_s, y_s = moe.moe_expert_ffn_static(*args, block_m=block_m)
+    h, y = moe.moe_expert_ffn(*args)
+    assert moe.moe_device_error()[0] == 0
+    assert torch.equal(h_s.view(torch.int16), h.view(torch.int16))
+    assert torch.equal(y_s, y)
+    _, y_or = _oracle_ffn(xp, offsets, wg, wu, wd)
+    assert np.linalg.norm(host_f64(y_s) - y_or) / np.linalg.norm(y_or) < 4e-3
+
+
 def test_dense_ffn_matches_plain_swiglu():
     xp, _, wg, wu, wd = _ffn_case([200], 512, 768)
     h, y = moe.moe_expert_ffn(dev_bf16(xp), None, dev_bf16(wg[0]), dev_bf16(wu[0]), dev_bf16(wd[0]))
