@@ -6,8 +6,10 @@ Python binding) never does, and shares no code with it.  It is plain numpy in
 float64, slow and written to be checked by eye against the method's
 definition.
 
-Parity unpinned: ``traffic_model_bytes`` (the fused/unfused byte model; the
-35 % figure the review quotes does not follow from the byte counts it prints).
+``traffic_model_bytes`` (the fused/unfused byte model) is pinned by counting
+the bytes an executed fused and unfused SwiGLU sequence moves; the 35 %
+figure the review quotes does not follow from the byte counts it prints and
+stays unreproduced (parity unpinned for that one figure).
 """
 from .moe_oracle import (  # noqa: F401
     Routing,
@@ -21,6 +23,7 @@ from .moe_oracle import (  # noqa: F401
     activate,
     swiglu_expert,
     combine,
+    route,
     forward,
     forward_tokens,
     dense_masked_forward,

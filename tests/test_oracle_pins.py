@@ -380,11 +380,98 @@ def test_invariants_on_real_workloads():
         assert np.array_equal(np.sort(p), np.arange(64 * wl.k))
 
 
-def test_traffic_model_arithmetic():
-    m = oracle.traffic_model_bytes(T=512, F=14336, d=4096)
-    assert m["unfused"] == 8 * 512 * 14336 + 4 * 512 * 4096
-    assert m["fused"] == 2 * 512 * 14336 + 2 * 512 * 4096
-    assert 0.70 < m["saving"] < 0.73  # not the 35 % the review quotes
+class _CountingMemory:
+    """A global memory that counts the bytes of every 16-bit tensor moved
+    through it, stored rounded to bf16-like width (2 bytes per element)."""
+
+    def __init__(self):
+        self.arrays, self.read, self.written = {}, 0, 0
+
+    def store(self, name, a):
+        self.arrays[name] = np.array(a, dtype=np.float64)
+        self.written += 2 * a.size
+
+    def load(self, name):
+        a = self.arrays[name]
+        self.read += 2 * a.size
+        return a
+
+    @property
+    def total(self):
+        return self.read + self.written
+
+
+def _run_unfused(x, wg, wu):
+    """Gate projection, up projection and activation as three passes through
+    global memory; returns (bytes before the activation's h write, bytes
+    with it, h)."""
+    m = _CountingMemory()
+    m.arrays["x"] = x  # already resident: the input itself is not an intermediate
+    m.store("g", m.load("x") @ wg.T)          # gate projection kernel
+    m.store("u", m.load("x") @ wu.T)          # up projection kernel
+    g, u = m.load("g"), m.load("u")           # activation kernel
+    h = g / (1.0 + np.exp(-g)) * u
+    before_h = m.total
+    m.store("h", h)
+    return before_h, m.total, h
+
+
+def _run_fused(x, wg, wu):
+    m = _CountingMemory()
+    m.arrays["x"] = x
+    xt = m.load("x")                          # one shared load of the input rows
+    g, u = xt @ wg.T, xt @ wu.T               # both projections from it, in registers
+    h = g / (1.0 + np.exp(-g)) * u
+    m.store("h", h)
+    return m.total, h
+
+
+@pytest.mark.parametrize("T,F,d", [(3, 5, 7), (16, 40, 12), (1, 9, 2), (11, 4, 30)])
+def test_traffic_model_against_executed_sequences(T, F, d):
+    """The byte model equals the bytes that executed fused and unfused SwiGLU
+    passes move through a counting memory (distinct T, F, d, so a dropped
+    term, a swapped dimension or a wrong coefficient fails)."""
+    rng = np.random.default_rng(T * 100 + F)
+    x, wg, wu = rng.normal(size=(T, d)), rng.normal(size=(F, d)), rng.normal(size=(F, d))
+    before_h, with_h, h_unf = _run_unfused(x, wg, wu)
+    fused, h_f = _run_fused(x, wg, wu)
+    np.testing.assert_allclose(h_unf, h_f, rtol=1e-12)  # both sequences compute the same h
+    np.testing.assert_allclose(h_f, oracle.activate(x @ wg.T) * (x @ wu.T), rtol=1e-12)
+    m = oracle.traffic_model_bytes(T=T, F=F, d=d)
+    assert m["unfused"] == before_h
+    assert m["unfused_with_h"] == with_h
+    assert m["fused"] == fused
+    assert m["saving"] == pytest.approx(1 - fused / before_h)
+    assert m["saving_with_h"] == pytest.approx(1 - fused / with_h)
+
+
+def test_traffic_model_saving_is_not_the_quoted_35_percent():
+    m = oracle.traffic_model_bytes(T=512, F=14336, d=4096)  # Mixtral-8x7B expert widths
+    assert 0.70 < m["saving"] < 0.73 and 0.76 < m["saving_with_h"] < 0.79
+
+
+# ----------------------------------------------------------------------------- teacher forcing
+
+def test_teacher_forced_choice_reweights_from_oracle_scores():
+    """A forced expert set is run with the oracle's own scores of those
+    experts: forcing the oracle's own choice changes nothing, and forcing
+    another set equals the brute-force mixture of those experts."""
+    wl, inp = _small(T=6, H=32, F=16, E=8, k=2)
+    free = oracle.forward(inp, wl)
+    same = oracle.forward(inp, wl, forced_idx=free["idx"])
+    np.testing.assert_array_equal(same["out"], free["out"])
+    forced = np.array([[7, 0], [1, 2], [3, 4], [5, 6], [0, 1], [2, 7]])
+    r = oracle.forward(inp, wl, forced_idx=forced)
+    xf = oracle.widen(inp["x"])
+    s = free["scores"]
+    for t in range(6):
+        w = s[t, forced[t]] / s[t, forced[t]].sum()
+        want = sum(w[j] * oracle.swiglu_expert(xf[t:t + 1], inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e])[0]
+                   for j, e in enumerate(forced[t]))
+        np.testing.assert_allclose(r["out"][t], want, rtol=1e-12, atol=1e-15)
+    np.testing.assert_array_equal(r["margin"], free["margin"])  # the margin stays the oracle's own
+    part = oracle.forward_tokens(inp, wl, [4, 1], forced_idx=forced[[4, 1]])
+    np.testing.assert_allclose(part["out"], r["out"][[4, 1]], rtol=1e-12, atol=1e-15)
 
 
 # ----------------------------------------------------------------------------- planted mistakes
