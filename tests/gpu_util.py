@@ -102,6 +102,91 @@ def compare_outputs(gpu_out: np.ndarray, orc_out: np.ndarray, what: str = "out")
     return rel, mx
 
 
+def seam_rows(counts, boxes=(512, 256, 128, 64), cap_per_expert=None) -> np.ndarray:
+    """Grouped rows where a token-tile bug would show: the first and last row
+    of every expert segment, and the rows on both sides of every boundary of
+    the balanced token tiles (ceil(r / box) tiles of equal rows rounded up to
+    16) an expert with r rows gets under each token box in ``boxes``.  With a
+    cap, an expert keeps its first rows in that order (ends, then the seams
+    of the larger boxes first)."""
+    rows = []
+    off = 0
+    for r in np.asarray(counts, dtype=np.int64).tolist():
+        if r > 0:
+            mine = [off, off + r - 1]
+            for bn in boxes:
+                ntb = -(-r // bn)
+                if ntb < 2:
+                    continue
+                tr = -(-(-(-r // ntb)) // 16) * 16
+                for b in range(tr, r, tr):
+                    mine += [off + b, off + b - 1]
+            mine = list(dict.fromkeys(mine))
+            if cap_per_expert is not None:
+                mine = mine[:cap_per_expert]
+            rows.extend(mine)
+        off += r
+    return np.unique(np.asarray(rows, dtype=np.int64))
+
+
+def tile_targeted_tokens(counts, perm, k, T, n_random=16, boxes=(512, 256, 128, 64), cap_per_expert=None,
+                         seed=11) -> np.ndarray:
+    """Tokens whose grouped rows sit on tile seams and segment ends (from the
+    GPU's own grouping: which rows are checked, not what they should hold),
+    plus the first and last token and n_random seeded random ones."""
+    rows = seam_rows(counts, boxes, cap_per_expert)
+    toks = np.asarray(perm)[rows] // k
+    import synth
+    rnd = (synth.uniform01(seed, 90, n_random) * T).astype(np.int64)
+    return np.unique(np.concatenate([toks, rnd, [0, T - 1]]).astype(np.int64))
+
+
+def check_forward(wl, inp: dict, d: dict, out: torch.Tensor, cfg, tokens=None, orc_route=None) -> dict:
+    """Parity of one layer forward with the oracle.
+
+    1. Routing of every token (check_routing).
+    2. Grouping: counts / offsets / perm / inv of the GPU's routing bit-exact
+       against the oracle's grouping of the GPU's indices, and against the
+       oracle's own grouping when every token picked the oracle's experts in
+       the oracle's slot order.
+    3. Output rows of ``tokens`` (every token when None; a callable is given
+       the GPU's counts and perm and returns the tokens) against the oracle
+       teacher-forced on the GPU's expert set for the tokens whose set
+       differs (near ties): their weights are the oracle's own scores of the
+       GPU's experts.  No row is left out.
+    Returns the statistics.
+    """
+    if tokens is not None and not callable(tokens) and len(tokens) == 0:
+        raise ValueError("no tokens to compare")
+    gidx_t, gw_t, _ = moe.moe_route(d["x"], d["w_router"], wl.k, cfg)
+    gidx, gw = gidx_t.cpu().numpy().astype(np.int64), gw_t.cpu().numpy()
+    orc = orc_route if orc_route is not None else oracle.route(inp, wl)
+    same = check_routing(wl, gidx, gw, orc)
+    counts, offsets, perm, inv, _ = moe.moe_permute(gidx_t, d["x"], wl.E)
+    c, o, p, i = (t.cpu().numpy().astype(np.int64) for t in (counts, offsets, perm, inv))
+    check_grouping(gidx, wl.E, c, o, p, i)
+    for got, want in zip((c, o, p, i), oracle.permute(gidx, wl.E)):
+        assert np.array_equal(got, want)
+    identical = np.array_equal(gidx, orc["idx"])
+    if identical:
+        for got, want in zip((c, o, p, i), oracle.permute(orc["idx"], wl.E)):
+            assert np.array_equal(got, want)
+    forced = np.where(same[:, None], orc["idx"], gidx)
+    if callable(tokens):
+        tokens = tokens(c, p)
+    if tokens is None:
+        ref = oracle.forward(inp, wl, forced_idx=forced)["out"]
+        got_out = host_f64(out)
+    else:
+        tokens = np.asarray(tokens, dtype=np.int64)
+        ref = oracle.forward_tokens(inp, wl, tokens, forced_idx=forced[tokens])["out"]
+        got_out = host_f64(out)[tokens]
+    assert np.all(np.isfinite(got_out))
+    rel, mx = compare_outputs(got_out, ref)
+    return {"rel_l2": rel, "max_abs": mx, "flipped": int((~same).sum()), "identical_routing": identical,
+            "rows_compared": int(got_out.shape[0]), "counts": c, "perm": p}
+
+
 def check_grouping(gpu_idx: np.ndarray, E: int, counts, offsets, perm, inv):
     """Properties of a correct stable grouping of the GPU's own routing."""
     T, k = gpu_idx.shape
