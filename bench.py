@@ -36,7 +36,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
-from synth.workloads import T_SWEEP  # noqa: E402
+from synth.workloads import SKEW_ALPHAS, T_SWEEP  # noqa: E402
 
 METRIC = "MoE layer fwd tokens/s on 1 GB300; % of max(HBM, bf16 tensor) roofline"
 NOMINAL_HBM = 8.0e12       # B/s, the layer roofline's denominators
@@ -222,6 +222,117 @@ def recorded_traffic(kernel: str, workload: str):
 
 # ----------------------------------------------------------------------------- our arm
 
+# Every (layer, T, alpha) point of the five layer shapes, timed in the same
+# run as the headline, in this order (one layer's weights on the device at a time).
+CONFIG_ORDER = ("deepseek", "mixtral", "qwen2", "skew", "tiny")
+
+
+def config_points():
+    pts = []
+    for name in CONFIG_ORDER:
+        for a in (SKEW_ALPHAS if name == "skew" else (None,)):
+            for T in T_SWEEP[name]:
+                pts.append((name, T, a))
+    return pts
+
+
+def to_device(torch, inp):
+    d = {}
+    for name, a in inp.items():
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+        d[name] = t.cuda().view(torch.bfloat16) if a.dtype == np.uint16 else t.cuda()
+    return d
+
+
+def load_workload(torch, wl_all):
+    """The layer's tensors on the device (one tensor generated on the host at
+    a time and dropped once copied)."""
+    d = to_device(torch, synth.make_inputs(wl_all, with_experts=False, with_shared=True))
+    for name in ("w_gate", "w_up", "w_down"):
+        shape = (wl_all.E, wl_all.F, wl_all.H) if name != "w_down" else (wl_all.E, wl_all.H, wl_all.F)
+        stream = {"w_gate": synth.STREAM_WG, "w_up": synth.STREAM_WU, "w_down": synth.STREAM_WD}[name]
+        d.update(to_device(torch, {name: synth.normal_bf16(wl_all.seed, stream, shape, std=0.02)}))
+    return d
+
+
+def time_point(moe, torch, d, cfg, wl, K, W, stream, world=1, timed_stages=True):
+    """K forwards of wl.T tokens back to back (after W warm-up forwards) on
+    `stream`, timed with CUDA events; per-stage times from events recorded by
+    the library between its stages."""
+    import torch.distributed as dist
+    T = wl.T
+    x = d["x"][:T]
+    out = torch.empty((T, wl.H), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(moe.moe_workspace_bytes(cfg, T, wl.H, wl.F, wl.E, wl.k), dtype=torch.uint8, device="cuda")
+
+    def fwd():
+        moe.moe_forward_ex(x, d["w_router"], d["w_gate"], d["w_up"], d["w_down"], wl.k, cfg, out=out,
+                           workspace=ws)
+
+    for _ in range(W):
+        fwd()
+    st, raw = moe.moe_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error {moe.moe_status_string(st)} {raw:#x}")
+    # active experts of this batch (for the compulsory-byte roofline)
+    idx, _, _ = moe.moe_route(x, d["w_router"], wl.k, cfg)
+    active = int(torch.unique(idx).numel())
+    ev = None
+    if timed_stages:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+        for row in ev:  # create the CUDA events before the timed region
+            for e in row:
+                e.record(stream)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(K):
+        if ev is not None:
+            moe.moe_set_trace_events(ev[i])
+        fwd()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    moe.moe_set_trace_events(None)
+    if world > 1:
+        dist.barrier()
+    ms = start.elapsed_time(stop)
+    res = {"T": T, "ms_total": ms, "active_experts": active, "wl": wl}
+    if ev is not None:
+        per = np.array([[ev[i][j].elapsed_time(ev[i][j + 1]) for j in range(5)] for i in range(K)])
+        res["stage_ms"] = dict(zip(STAGES, per.mean(axis=0).tolist()))
+    st, raw = moe.moe_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error {moe.moe_status_string(st)} {raw:#x}")
+    del out, ws
+    return res
+
+
+def point_summary(r, K):
+    w = r["wl"]
+    ms = r["ms_total"] / K
+    tr = max(w.flops() / NOMINAL_BF16, w.compulsory_bytes(r["active_experts"]) / NOMINAL_HBM)
+    out = {"workload": w.label, "T": w.T, "tokens_per_s": w.T / (ms / 1e3), "us_per_step": ms * 1e3,
+           "layer_roofline_us": tr * 1e6, "layer_roofline_frac": tr / (ms / 1e3),
+           "active_experts": r["active_experts"], "steps": K}
+    if w.alpha is not None:
+        out["alpha"] = w.alpha
+    if "stage_ms" in r:
+        out["stages_us"] = {k2: v * 1e3 for k2, v in r["stage_ms"].items()}
+    return out
+
+
+def skew_slowdown(configs):
+    """Per T of the skew layer: time per forward at alpha = 2 over alpha = 0."""
+    by = {(c["T"], c.get("alpha")): c["us_per_step"] for c in configs if c["workload"].startswith("skew")}
+    res = {}
+    for (T, a), us in sorted(by.items()):
+        if a == 2.0 and (T, 0.0) in by:
+            res[str(T)] = us / by[(T, 0.0)]
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -237,70 +348,16 @@ def run_ours(args):
 
     kw = workload_overrides(args)
     T_main = args.T if args.T is not None else max(T_SWEEP[args.workload])
-    sweep_T = [] if args.no_sweep else [t for t in T_SWEEP[args.workload] if t != T_main]
-    T_all = max([T_main] + sweep_T)
+    T_all = max([T_main] + list(T_SWEEP[args.workload]))
     wl_all = synth.workload(args.workload, T=T_all, **kw)
-    inp = synth.make_inputs(wl_all)
-    d = {}
-    for name, a in inp.items():
-        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
-        d[name] = t.cuda().view(torch.bfloat16) if a.dtype == np.uint16 else t.cuda()
+    d = load_workload(torch, wl_all)
     cfg = make_cfg(moe, wl_all, d)
-    weight_bytes_per_expert = 6.0 * wl_all.H * wl_all.F
-
-    def run_T(T, K, W, timed_stages):
-        wl = wl_all.with_T(T)
-        x = d["x"][:T]
-        out = torch.empty((T, wl.H), dtype=torch.bfloat16, device="cuda")
-        ws = torch.empty(moe.moe_workspace_bytes(cfg, T, wl.H, wl.F, wl.E, wl.k), dtype=torch.uint8, device="cuda")
-
-        def fwd():
-            moe.moe_forward_ex(x, d["w_router"], d["w_gate"], d["w_up"], d["w_down"], wl.k, cfg, out=out,
-                               workspace=ws)
-
-        for _ in range(W):
-            fwd()
-        st, raw = moe.moe_device_error()
-        if st != 0:
-            raise RuntimeError(f"device error {moe.moe_status_string(st)} {raw:#x}")
-        # active experts of this batch (for the compulsory-byte roofline)
-        idx, _, _ = moe.moe_route(x, d["w_router"], wl.k, cfg)
-        active = int(torch.unique(idx).numel())
-        ev = None
-        if timed_stages:
-            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
-            for row in ev:  # create the CUDA events before the timed region
-                for e in row:
-                    e.record(stream)
-        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        start.record(stream)
-        for i in range(K):
-            if ev is not None:
-                moe.moe_set_trace_events(ev[i])
-            fwd()
-        stop.record(stream)
-        torch.cuda.synchronize()
-        moe.moe_set_trace_events(None)
-        if world > 1:
-            dist.barrier()
-        ms = start.elapsed_time(stop)
-        res = {"T": T, "ms_total": ms, "active_experts": active, "wl": wl}
-        if ev is not None:
-            per = np.array([[ev[i][j].elapsed_time(ev[i][j + 1]) for j in range(5)] for i in range(K)])
-            res["stage_ms"] = dict(zip(STAGES, per.mean(axis=0).tolist()))
-        st, raw = moe.moe_device_error()
-        if st != 0:
-            raise RuntimeError(f"device error {moe.moe_status_string(st)} {raw:#x}")
-        return res
 
     pk, pk_kind = peaks()
     # clocks over the headline batch's timed forwards and its end-to-end leg
     clocks = ClockSampler(local).__enter__()
     try:
-        main = run_T(T_main, args.steps, args.warmup, True)
+        main = time_point(moe, torch, d, cfg, wl_all.with_T(T_main), args.steps, args.warmup, stream, world)
     except BaseException:
         clocks.__exit__(None, None, None)
         raise
@@ -344,30 +401,50 @@ def run_ours(args):
     roof["peak_source"] = f"{pk_kind} ({kind if roof['bound'] == 'tensor' else 'copy'})"
     roof["kernel"] = dom
     roof["traffic"] = recorded_traffic(dom, wl.label)
-    roof["algorithmic"] = {"flops_per_launch": f_dom, "bytes_per_launch": b_dom}
+    roof["algorithmic"] = {"flops_per_launch": f_dom, "bytes_per_launch": b_dom,
+                           "intensity_flop_per_byte": intensity, "ridge_flop_per_byte": ridge}
+    gpu_launches = moe.moe_forward_launches(cfg, wl.T, wl.H, wl.F, wl.E, wl.k) * args.steps
 
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(wl, budget_s=args.cpu_seconds)
 
-    sweep = []
-    for T in sweep_T:
-        K = max(args.steps, 20) if T <= 32 else args.steps
-        r = run_T(T, K, args.warmup, True)
-        w = r["wl"]
-        ms = r["ms_total"] / K
-        tr = max(w.flops() / NOMINAL_BF16, w.compulsory_bytes(r["active_experts"]) / NOMINAL_HBM)
-        sweep.append({"T": T, "tokens_per_s": T / (ms / 1e3), "us_per_step": ms * 1e3,
-                      "layer_roofline_frac": tr / (ms / 1e3), "active_experts": r["active_experts"],
-                      "stages_us": {k2: v * 1e3 for k2, v in r["stage_ms"].items()}})
+    # every point of the five layer shapes, in the same run
+    configs, decode = [], []
+    headline_key = (args.workload, T_main, wl.alpha)
+    if not args.no_sweep and not kw.get("E") and not kw.get("activation"):
+        loaded = (args.workload, wl.alpha)
+        for name, T, a in config_points():
+            if (name, T, a) == headline_key:
+                configs.append(dict(point_summary(main, args.steps), headline=True))
+                continue
+            if (name, a) != loaded:
+                del d
+                torch.cuda.empty_cache()
+                wl_all = synth.workload(name, T=max(T_SWEEP[name]), **({} if a is None else {"alpha": a}))
+                d = load_workload(torch, wl_all)
+                cfg = make_cfg(moe, wl_all, d)
+                loaded = (name, a)
+            K = max(args.steps, 50) if T <= 32 else max(args.steps, 20) if T <= 512 else args.steps
+            r = time_point(moe, torch, d, cfg, wl_all.with_T(T), K, args.warmup, stream, world)
+            configs.append(point_summary(r, K))
+            if name == "mixtral" and T == max(T_SWEEP[name]) and not args.no_decode:
+                decode = run_decode(moe, torch, d, cfg, wl_all, stream)
 
-    decode = [] if (args.no_decode or args.no_sweep) else run_decode(moe, torch, d, cfg, wl_all, stream)
     esweep = run_expert_sweep(moe, torch, args, stream) if args.expert_sweep else None
-    sched = None
-    if args.schedule_ablation:
-        sched = run_schedule_ablation(moe, torch, d, cfg, wl_all, sorted(set([T_main] + sweep_T)), stream,
-                                      args.steps)
-    ablation = None
-    if args.fusion_ablation:
-        ablation = run_fusion_ablation(moe, torch, d, cfg, wl_all, sorted(set([T_main] + sweep_T)), stream,
-                                       args.steps)
+    sched = ablation = None
+    if args.schedule_ablation or args.fusion_ablation:
+        if (wl_all.name, wl_all.alpha) != (args.workload, wl.alpha):
+            del d
+            torch.cuda.empty_cache()
+            wl_all = synth.workload(args.workload, T=T_all, **kw)
+            d = load_workload(torch, wl_all)
+            cfg = make_cfg(moe, wl_all, d)
+        Ts = sorted(set([T_main] + list(T_SWEEP[args.workload])))
+        if args.schedule_ablation:
+            sched = run_schedule_ablation(moe, torch, d, cfg, wl_all, Ts, stream, args.steps)
+        if args.fusion_ablation:
+            ablation = run_fusion_ablation(moe, torch, d, cfg, wl_all, Ts, stream, args.steps)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -385,8 +462,9 @@ def run_ours(args):
         "stages_ms": stage_ms,
         "e2e": e2e,
         "clocks": clk,
-        "gpu_launches": launches_per_forward(wl) * args.steps,
-        "sweep": sweep,
+        "gpu_launches": gpu_launches,
+        "configs": configs,
+        "skew_alpha2_over_alpha0_time": skew_slowdown(configs),
         "decode": decode,
     }
     if esweep is not None:
@@ -395,8 +473,8 @@ def run_ours(args):
         line["fusion_ablation"] = ablation
     if sched is not None:
         line["schedule_ablation"] = sched
-    if rank == 0 and not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(wl, inp, budget_s=args.cpu_seconds)
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -488,12 +566,7 @@ def run_expert_sweep(moe, torch, args, stream):
     res = []
     for E in EXPERT_SWEEP_E:
         wl_all = expert_sweep(E, max(ESWEEP_T))
-        inp = synth.make_inputs(wl_all)
-        d = {}
-        for name, a in inp.items():
-            t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
-            d[name] = t.cuda().view(torch.bfloat16) if a.dtype == np.uint16 else t.cuda()
-        del inp
+        d = load_workload(torch, wl_all)
         cfg = make_cfg(moe, wl_all, d)
         for T in ESWEEP_T:
             wl = wl_all.with_T(T)
@@ -653,17 +726,30 @@ def run_e2e(moe, torch, d, cfg, wl, args, stream):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def cpu_baseline(wl, inp, budget_s=15.0, sample_tokens=4):
+def oracle_inputs(wl):
+    """Host inputs for the oracle without the routed experts' weights (those
+    are generated one expert at a time by expert_weights)."""
+    inp = synth.make_inputs(wl, with_experts=False, with_shared=True)
+
+    def expert_weights(name, e):
+        return synth.expert_slice(wl, name, e)
+    return inp, expert_weights
+
+
+def cpu_baseline(wl, budget_s=15.0, sample_tokens=4):
     """The oracle, as it stands, on the host cores: forward_tokens over
-    consecutive samples of the batch until about budget_s seconds pass."""
+    consecutive samples of the batch until about budget_s seconds pass (the
+    experts' weights generated per call, as the oracle's expert_weights hook
+    allows; generation included in the time)."""
     import oracle
 
+    inp, ew = oracle_inputs(wl)
     t0 = time.perf_counter()
     done = 0
     start = 0
     while time.perf_counter() - t0 < budget_s and done < wl.T:
         toks = np.arange(start, min(start + sample_tokens, wl.T))
-        oracle.forward_tokens(inp, wl, toks)
+        oracle.forward_tokens(inp, wl, toks, expert_weights=ew)
         done += toks.size
         start += toks.size
     el = time.perf_counter() - t0
@@ -681,12 +767,12 @@ def run_reference(args):
     kw = workload_overrides(args)
     T = args.T if args.T is not None else max(T_SWEEP[args.workload])
     wl = synth.workload(args.workload, T=T, **kw)
-    inp = synth.make_inputs(wl)
-    n = 4
+    inp, ew = oracle_inputs(wl)
+    n = 4 if wl.E * wl.F * wl.H < 2e10 else 1
 
     def step(i):
         toks = (np.arange(n) + i * n) % wl.T
-        oracle.forward_tokens(inp, wl, toks)
+        oracle.forward_tokens(inp, wl, toks, expert_weights=ew)
 
     for i in range(args.warmup):
         step(i)
@@ -712,7 +798,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="mixtral", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="deepseek", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--alpha", type=float, default=None)
     ap.add_argument("--activation", default=None, choices=["silu", "gelu"],
@@ -720,7 +806,8 @@ def main():
     ap.add_argument("--experts", type=int, default=None,
                     help="reduced expert count (same H, F, k, routing) for small profiling captures")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="time only the headline batch (not every point of the five layer shapes)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--schedule-ablation", action="store_true",
                     help="also time the persistent device schedule against host-read counts, fixed 64-row "
@@ -730,7 +817,8 @@ def main():
     ap.add_argument("--expert-sweep", action="store_true",
                     help="also time the expert-count sweep (E = 8..128, F = 8*14336/E, H = 4096, top-2)")
     ap.add_argument("--no-decode", action="store_true",
-                    help="skip the eager vs CUDA-graph decode-size timings (also skipped with --no-sweep)")
+                    help="skip the eager vs CUDA-graph decode-size timings on the Mixtral-shaped layer (also "
+                         "skipped with --no-sweep)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:

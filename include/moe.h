@@ -261,14 +261,33 @@ MOE_API moe_status_t moe_forward_ex(const moe_config_t* cfg, const void* x, cons
 
 /*
  * moe_forward_ex with the Mixtral routing (moe_config_default) and a
- * workspace the library keeps per device, grown with cudaMallocAsync on
- * `stream` when a larger call arrives.  Calls that run concurrently on
- * different streams of one device must use moe_forward_ex with their own
- * workspaces instead.
+ * workspace the library keeps per device, grown (cudaFreeAsync of the old
+ * one, cudaMallocAsync of the new one, both on `stream`) when a larger call
+ * arrives.  Calls on one device are ordered through an event the library
+ * records after each call: a call's work waits for the previous call's work,
+ * on whatever stream it ran, so the shared workspace is never used by two
+ * calls at once nor freed under a call still running.  Calls on different
+ * streams therefore serialise on the device; callers that want them to
+ * overlap use moe_forward_ex with their own workspaces.  Not for stream
+ * capture (returns MOE_ERR_UNSUPPORTED on a capturing stream): capture
+ * moe_forward_ex with a caller workspace instead.
  */
 MOE_API moe_status_t moe_forward(const void* x, const void* w_router, const void* w_gate,
                          const void* w_up, const void* w_down, int T, int H, int F, int E,
                          int k, void* out, moe_stream_t stream);
+
+/*
+ * How many kernels one moe_forward_ex / moe_forward call launches for these
+ * shapes and this configuration (cfg NULL: the defaults), or -1 if the
+ * arguments would be rejected.  Host only, no device work.
+ */
+MOE_API int moe_forward_launches(const moe_config_t* cfg, int T, int H, int F, int E, int k);
+
+/*
+ * Kernels this library has launched since it was loaded (all entry points,
+ * all devices; a host-side count of successful launches).
+ */
+MOE_API unsigned long long moe_launches_issued(void);
 
 /* Human-readable name of a status code (static storage). */
 MOE_API const char* moe_status_string(moe_status_t status);

@@ -20,7 +20,7 @@ __all__ = [
     "moe_permute_scratch_bytes", "moe_permute_noalloc", "moe_expert_ffn", "moe_expert_ffn_unfused",
     "moe_expert_ffn_static", "moe_combine", "moe_workspace_bytes", "moe_forward_ex",
     "moe_forward", "moe_device_error", "moe_set_trace_events", "moe_selftest_wait_timeout", "moe_status_string",
-    "EXPORTED_SYMBOLS",
+    "moe_forward_launches", "moe_launches_issued", "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -33,6 +33,7 @@ EXPORTED_SYMBOLS = (
     "moe_combine", "moe_workspace_bytes", "moe_forward_ex", "moe_forward", "moe_status_string",
     "moe_device_error", "moe_set_trace_events", "moe_selftest_wait_timeout", "moe_abi_version",
     "moe_permute_noalloc", "moe_expert_ffn_ex", "moe_expert_ffn_unfused", "moe_expert_ffn_static",
+    "moe_forward_launches", "moe_launches_issued",
 )
 
 ACTIVATIONS = {"silu": 0, "gelu": 1}  # moe_activation_t
@@ -118,6 +119,8 @@ def load_library():
         "moe_set_trace_events": (I, [P, I]),
         "moe_selftest_wait_timeout": (I, [U, P]),
         "moe_abi_version": (I, []),
+        "moe_forward_launches": (I, [P, I, I, I, I, I]),
+        "moe_launches_issued": (ctypes.c_ulonglong, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -342,6 +345,16 @@ def moe_forward(x, w_router, w_gate, w_up, w_down, k, out=None, stream=None):
                          _stream(stream))
     _check(st, "moe_forward")
     return out
+
+
+def moe_forward_launches(cfg: MoeConfig | None, T, H, F, E, k) -> int:
+    """Kernels one moe_forward_ex call launches for these shapes (-1: rejected arguments)."""
+    return int(load_library().moe_forward_launches(ctypes.byref(cfg) if cfg is not None else None, T, H, F, E, k))
+
+
+def moe_launches_issued() -> int:
+    """Kernels the library has launched since it was loaded."""
+    return int(load_library().moe_launches_issued())
 
 
 def moe_set_trace_events(events):

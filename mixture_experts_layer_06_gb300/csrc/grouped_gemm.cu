@@ -41,6 +41,10 @@ namespace {
 #ifndef MOE_EXACT_N
 #define MOE_EXACT_N 1
 #endif
+// Stages of L2 prefetch lookahead for the weight boxes (0: off).
+#ifndef MOE_PF_DIST
+#define MOE_PF_DIST 0
+#endif
 
 constexpr int kThreads = 192;
 constexpr int kMaxStages = 8;
@@ -285,6 +289,41 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
         tma_prefetch_map(&maps.seg[sg].b);
       }
       bool ok = true;
+#if MOE_PF_DIST > 0
+      // L2 prefetch of the weight boxes MOE_PF_DIST stages ahead of the loads,
+      // so that more weight bytes are in flight from DRAM than the shared
+      // memory ring holds (multi-K-block stages with the TMA box views only).
+      int pf_tile = first, pf_kb = 0;
+      Tile pt{};
+      bool pf_on = pf_tile < total;
+      if (pf_on) {
+        pt = decode_tile(a, sc, pf_tile);
+        pf_kb = pt.kb0;
+      }
+      auto pf_step = [&]() {
+        while (pf_on && pf_kb >= pt.kb1) {
+          pf_tile += stride;
+          pf_on = pf_tile < total;
+          if (pf_on) {
+            pt = decode_tile(a, sc, pf_tile);
+            pf_kb = pt.kb0;
+          }
+        }
+        if (!pf_on) return;
+        if (KPS > 1 && !(SWIGLU && a.seg[pt.s].a_mode == kTwoMaps)) {
+          const CUtensorMap* am = &maps.seg[pt.s].a0;
+          const int ar = pt.a_row + static_cast<int>(rank) * FEAT * NSUB;
+          for (int u = 0; u < NSUB; ++u) {
+            if (SWIGLU)
+              tma_prefetch_4d(am, 0, ar + u * kHalfRows, 0, pf_kb * KPS);
+            else
+              tma_prefetch_3d(am, 0, ar + u * kTileM, pf_kb * KPS);
+          }
+        }
+        ++pf_kb;
+      };
+      for (int i = 0; i < MOE_PF_DIST; ++i) pf_step();
+#endif
       for (int tile = first; tile < total && ok; tile += stride) {
         const Tile t = decode_tile(a, sc, tile);
         const SegMaps& ms = maps.seg[t.s];
@@ -302,6 +341,9 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
           }
           uint8_t* st = smem + s * stage_bytes;
           uint8_t* sb = st + KPS * NSUB * kATileBytes;
+#if MOE_PF_DIST > 0
+          pf_step();
+#endif
           if (PAIR) {
             if (rank == 0) mbar_arrive_expect_tx(&full[s], bytes);
             const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);

@@ -1,6 +1,7 @@
 // Host-side launchers of the MoE kernels (internal to the library).
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -15,6 +16,9 @@ namespace moe {
 #ifndef MOE_PDL
 #define MOE_PDL 1
 #endif
+// Kernels launched through launch_kernel since the library was loaded.
+extern std::atomic<unsigned long long> g_launch_count;
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                           Args&&... args) {
@@ -28,7 +32,9 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   attr[0].val.programmaticStreamSerializationAllowed = MOE_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  if (e == cudaSuccess) g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  return e;
 }
 
 // Routing variant as the kernels see it.

@@ -15,6 +15,8 @@
 // Device error word (bit 0 timeout, bit 1 bounds, bits 8.. sites).
 __device__ uint32_t g_moe_error_word;
 
+std::atomic<unsigned long long> moe::g_launch_count{0};
+
 // One thread waits on an mbarrier that nothing ever arrives on; the bounded
 // wait must give up after limit_ns and record a timeout (failure-path check).
 __global__ void selftest_wait_kernel(uint64_t limit_ns, uint32_t* err) {
@@ -42,9 +44,11 @@ struct DeviceState {
   int num_sms = 0;
   void* ws = nullptr;  // moe_forward's cached workspace
   size_t ws_bytes = 0;
+  cudaEvent_t ws_done = nullptr;  // recorded after the last moe_forward call's work
 };
 
 std::mutex g_mutex;
+std::mutex g_ws_mutex;  // moe_forward's workspace: held while a call is enqueued
 DeviceState g_dev[kMaxDevices];
 EncodeTiledFn g_encode = nullptr;
 
@@ -511,6 +515,17 @@ moe_status_t ffn_static_impl(DeviceState* d, const FfnOperands& o, int block_m, 
   return MOE_OK;
 }
 
+// Kernels moe_forward_ex launches for these shapes (its launch sequence below).
+int forward_launches(const moe_config_t& c, int T, int H, int E) {
+  if (T == 0) return 0;
+  const moe::RouterPlan rp = moe::router_plan(T, H, E, c.w_shared_gate != nullptr);
+  const int route = 2 + ((c.w_shared_gate != nullptr && !rp.fused_gate) ? 1 : 0);
+  const int permute = 3;
+  const int ffn = 2;
+  const int combine = 1;
+  return route + permute + ffn + combine;
+}
+
 }  // namespace
 
 namespace moe {
@@ -534,7 +549,7 @@ void moe_config_default(moe_config_t* cfg) {
   cfg->activation = MOE_ACT_SILU;
 }
 
-int moe_abi_version(void) { return 101; }
+int moe_abi_version(void) { return 102; }
 
 moe_status_t moe_set_trace_events(void* const* events, int count) {
   if (events == nullptr || count == 0) {
@@ -775,20 +790,39 @@ moe_status_t moe_forward(const void* x, const void* w_router, const void* w_gate
   if ((st = device_state(&d)) != MOE_OK) return st;
   const size_t need = layout(c, T, H, F, E, k).total;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  void* ws = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (d->ws_bytes < need) {
-      if (d->ws != nullptr && cudaFreeAsync(d->ws, s) != cudaSuccess) return MOE_ERR_CUDA;
-      d->ws = nullptr;
-      d->ws_bytes = 0;
-      if (cudaMallocAsync(&d->ws, need, s) != cudaSuccess) return MOE_ERR_CUDA;
-      d->ws_bytes = need;
-    }
-    ws = d->ws;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cap != cudaStreamCaptureStatusNone) return MOE_ERR_UNSUPPORTED;  // moe_forward_ex is the capturable form
+  // Calls are ordered through ws_done: each call's work waits for the previous
+  // call's work (on whatever stream it ran), so the one workspace is never
+  // used by two calls at once and is never freed under a call still running.
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  if (d->ws_done == nullptr && cudaEventCreateWithFlags(&d->ws_done, cudaEventDisableTiming) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamWaitEvent(s, d->ws_done, 0) != cudaSuccess) return MOE_ERR_CUDA;
+  if (d->ws_bytes < need) {
+    if (d->ws != nullptr && cudaFreeAsync(d->ws, s) != cudaSuccess) return MOE_ERR_CUDA;
+    d->ws = nullptr;
+    d->ws_bytes = 0;
+    if (cudaMallocAsync(&d->ws, need, s) != cudaSuccess) return MOE_ERR_CUDA;
+    d->ws_bytes = need;
   }
-  return moe_forward_ex(&c, x, w_router, w_gate, w_up, w_down, T, H, F, E, k, out, ws, need, stream);
+  st = moe_forward_ex(&c, x, w_router, w_gate, w_up, w_down, T, H, F, E, k, out, d->ws, need, stream);
+  if (cudaEventRecord(d->ws_done, s) != cudaSuccess && st == MOE_OK) st = MOE_ERR_CUDA;
+  return st;
 }
+
+int moe_forward_launches(const moe_config_t* cfg, int T, int H, int F, int E, int k) {
+  moe_config_t c;
+  if (cfg)
+    c = *cfg;
+  else
+    moe_config_default(&c);
+  if (check_dims(T, H, F, E, k) != MOE_OK || check_config(c, H, E, k) != MOE_OK) return -1;
+  return forward_launches(c, T, H, E);
+}
+
+unsigned long long moe_launches_issued(void) { return moe::g_launch_count.load(std::memory_order_relaxed); }
 
 moe_status_t moe_selftest_wait_timeout(uint32_t limit_us, moe_stream_t stream) {
   if (limit_us == 0 || limit_us > 1000000u) return MOE_ERR_INVALID_VALUE;

@@ -242,10 +242,14 @@ extern "C" MOE_API moe_status_t moe_permute_noalloc(const int32_t* topk_idx, con
     if (cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }
+  // The device error word must exist before anything is launched: without it
+  // an out-of-range expert id would be dropped silently.
+  uint32_t* err = moe::device_error_word();
+  if (err == nullptr) return MOE_ERR_CUDA;
   // Every scratch word the kernels read is written earlier in the same call
   // (bitmap_kernel writes all ceil(T/32) * E bitmap words, scan_kernel all
   // row bases), so nothing needs clearing between calls.
   const cudaError_t e = moe::launch_permute(topk_idx, x, T, H, E, k, counts, offsets, perm, inv, x_perm, scratch,
-                                            moe::device_error_word(), s);
+                                            err, s);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

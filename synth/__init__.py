@@ -163,13 +163,14 @@ def random_topk(seed: int, T: int, E: int, k: int, alpha: float = 0.0,
     return order.astype(np.int32)
 
 
-def make_inputs(wl: Workload, with_experts: bool = True) -> dict:
+def make_inputs(wl: Workload, with_experts: bool = True, with_shared: bool = False) -> dict:
     """All tensors of one workload as numpy arrays (bf16 as uint16 bit patterns).
 
     x ~ N(0,1); every weight ~ N(0, 0.02); router bias (skew only) fp32.
     The tensor for stream s holds element i = index i of stream s of wl.seed,
     so an expert's slice e of a [E, rows, cols] weight is elements
-    e*rows*cols ... of that stream.
+    e*rows*cols ... of that stream.  with_experts=False leaves out the routed
+    experts' weights (and, unless with_shared, the shared expert's).
     """
     s = wl.seed
     d = {"x": normal_bf16(s, STREAM_X, (wl.T, wl.H)),
@@ -178,10 +179,10 @@ def make_inputs(wl: Workload, with_experts: bool = True) -> dict:
         d["w_gate"] = normal_bf16(s, STREAM_WG, (wl.E, wl.F, wl.H), std=0.02)
         d["w_up"] = normal_bf16(s, STREAM_WU, (wl.E, wl.F, wl.H), std=0.02)
         d["w_down"] = normal_bf16(s, STREAM_WD, (wl.E, wl.H, wl.F), std=0.02)
-        if wl.F_shared:
-            d["ws_gate"] = normal_bf16(s, STREAM_WSG, (wl.F_shared, wl.H), std=0.02)
-            d["ws_up"] = normal_bf16(s, STREAM_WSU, (wl.F_shared, wl.H), std=0.02)
-            d["ws_down"] = normal_bf16(s, STREAM_WSD, (wl.H, wl.F_shared), std=0.02)
+    if wl.F_shared and (with_experts or with_shared):
+        d["ws_gate"] = normal_bf16(s, STREAM_WSG, (wl.F_shared, wl.H), std=0.02)
+        d["ws_up"] = normal_bf16(s, STREAM_WSU, (wl.F_shared, wl.H), std=0.02)
+        d["ws_down"] = normal_bf16(s, STREAM_WSD, (wl.H, wl.F_shared), std=0.02)
     if wl.shared_gate:
         d["w_shared_gate"] = normal_bf16(s, STREAM_WSGATE, (wl.H,), std=0.02)
     if wl.alpha is not None:

@@ -22,7 +22,7 @@ static int failures = 0;
   } while (0)
 
 int main(void) {
-  CHECK(moe_abi_version() == 101);
+  CHECK(moe_abi_version() == 102);
 
   moe_config_t cfg;
   memset(&cfg, 0x5A, sizeof cfg);

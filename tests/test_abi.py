@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.moe_abi_version() == 101
+    assert lib.moe_abi_version() == 102
     assert moe.moe_status_string(0) == "MOE_OK"
     assert moe.moe_status_string(6) == "MOE_ERR_DEVICE_BOUNDS"
     assert moe.moe_status_string(99) == "MOE_ERR_UNKNOWN"
@@ -139,3 +139,12 @@ def test_route_scratch_checked_before_launch(lib):
     assert lib.moe_route(None, 0x1000, 0x2000, 4, 512, 8, 2, 0x3000, 0x4000, None, 0x5000, need - 1, None) == 3
     assert lib.moe_route(None, 0x1000, 0x2000, 4, 512, 8, 2, 0x3000, 0x4000, None, None, need, None) == 1
     assert lib.moe_route_scratch_bytes(None, 4, 500, 8) == 0
+
+
+def test_forward_launch_query_on_the_host(lib):
+    # tiny layer: router GEMM + top-k, three permute launches, two GEMMs, combine
+    n = moe.moe_forward_launches(None, 128, 512, 1024, 8, 2)
+    assert 4 <= n <= 12
+    assert moe.moe_forward_launches(None, 0, 512, 1024, 8, 2) == 0  # T = 0 launches nothing
+    assert moe.moe_forward_launches(None, 128, 500, 1024, 8, 2) == -1  # rejected shape
+    assert moe.moe_launches_issued() >= 0
