@@ -134,33 +134,27 @@ def make_cfg(moe, wl, d):
                               activation=wl.activation)
 
 
-def launches_per_forward(wl) -> int:
-    # router GEMM, top-k, bitmap, scan, gather, gate+up GEMM, down GEMM, combine; a separate
-    # shared-gate launch only when the gate row does not fit the router GEMM (E rounded to 16 > 240)
-    separate_gate = wl.shared_gate and (wl.E + 15) // 16 * 16 + 16 > 256
-    return 8 + (1 if separate_gate else 0)
-
-
 def stage_algorithmic(wl, active: int):
     """Algorithmic FLOPs and bytes of each stage of one forward: what the
-    stage must compute and move at minimum given its inputs and outputs."""
+    stage must compute and move at minimum given its inputs and outputs
+    (x_perm and h bf16, the expert outputs y fp16)."""
     T, H, F, E, k = wl.T, wl.H, wl.F, wl.E, wl.k
     Tk = T * k
     out = {
         "route": (2.0 * T * H * E, T * H * 2.0 + E * H * 2.0 + Tk * 8.0),
         "permute": (0.0, T * H * 2.0 + Tk * H * 2.0 + Tk * 12.0),
         "gate_up_gemm": (Tk * 4.0 * H * F, active * 4.0 * H * F + Tk * H * 2.0 + Tk * F * 2.0),
-        "down_gemm": (Tk * 2.0 * H * F, active * 2.0 * H * F + Tk * F * 2.0 + Tk * H * 4.0),
-        "combine": (0.0, Tk * H * 4.0 + T * H * 2.0 + Tk * 8.0),
+        "down_gemm": (Tk * 2.0 * H * F, active * 2.0 * H * F + Tk * F * 2.0 + Tk * H * 2.0),
+        "combine": (0.0, Tk * H * 2.0 + T * H * 2.0 + Tk * 8.0),
     }
     if wl.F_shared:
         Fs = wl.F_shared
         f, b = out["gate_up_gemm"]
         out["gate_up_gemm"] = (f + T * 4.0 * H * Fs, b + 4.0 * H * Fs + T * H * 2.0 + T * Fs * 2.0)
         f, b = out["down_gemm"]
-        out["down_gemm"] = (f + T * 2.0 * H * Fs, b + 2.0 * H * Fs + T * Fs * 2.0 + T * H * 4.0)
+        out["down_gemm"] = (f + T * 2.0 * H * Fs, b + 2.0 * H * Fs + T * Fs * 2.0 + T * H * 2.0)
         f, b = out["combine"]
-        out["combine"] = (f, b + T * H * 4.0)
+        out["combine"] = (f, b + T * H * 2.0)
     return out
 
 
@@ -662,7 +656,8 @@ def run_decode(moe, torch, d, cfg, wl_all, stream, reps=200):
         if st != 0:
             raise RuntimeError(f"device error {moe.moe_status_string(st)} {raw:#x}")
         res.append({"T": T, "eager_us": eager_us, "graph_us": graph_us, "host_issue_us": host_us,
-                    "graph_bitwise_equal": same, "launches": launches_per_forward(wl)})
+                    "graph_bitwise_equal": same,
+                    "launches": moe.moe_forward_launches(cfg, T, wl.H, wl.F, wl.E, wl.k)})
         del g
     return res
 

@@ -109,8 +109,9 @@ MOE_API void moe_config_default(moe_config_t* cfg);
 /*
  * Router scoring and top-k selection ("The reading": tokens are scored).
  * logits = x . W_r^T (+ logit_bias) with fp32 accumulation on the tensor
- * cores (the K dimension split over CTAs, partial logits added in a fixed
- * order), then the score function, top-k and weights as in moe_config_t.
+ * cores (the K dimension split over the CTAs of a thread-block cluster, the
+ * partial logits added in rank order in shared memory), then the score
+ * function, top-k and weights as in moe_config_t, in the same launch.
  *   x:            bf16 [T, H]
  *   w_router:     bf16 [E, H]
  *   topk_idx:     int32 [T, k] out, slot order = descending score
@@ -118,8 +119,10 @@ MOE_API void moe_config_default(moe_config_t* cfg);
  *   shared_scale: fp32 [T] out, sigmoid(x . w_shared_gate); may be NULL
  *                 when cfg->w_shared_gate is NULL.
  *   scratch:      device memory of at least moe_route_scratch_bytes(cfg, T,
- *                 H, E) bytes (fp32 partial logits); too little returns
- *                 MOE_ERR_WORKSPACE.
+ *                 H, E) bytes; too little returns MOE_ERR_WORKSPACE.  This
+ *                 version needs none (moe_route_scratch_bytes returns 0), so
+ *                 scratch may be NULL; the argument stays for callers that
+ *                 size it from moe_route_scratch_bytes.
  * cfg may be NULL (moe_config_default).
  */
 MOE_API size_t moe_route_scratch_bytes(const moe_config_t* cfg, int T, int H, int E);
@@ -182,19 +185,23 @@ MOE_API moe_status_t moe_permute_noalloc(const int32_t* topk_idx, const void* x,
  *            (then E must be 1: a dense SwiGLU MLP, used for shared experts)
  *   w_gate, w_up: bf16 [E, F, H];  w_down: bf16 [E, H, F]
  *   h:       bf16 [rows, F] out, SiLU(x W_gate^T) * (x W_up^T) rounded to bf16
- *   y:       fp32 [rows, H] out, h W_down^T
+ *   y:       fp16 [rows, H] out, h W_down^T accumulated in fp32 and rounded
+ *            once to fp16 (a 16-bit intermediate, as the pages' byte model
+ *            counts; fp16 rather than bf16 for its 8x finer rounding).  A
+ *            value beyond the fp16 range (|y| > 65504) becomes inf and sets
+ *            MOE_ERR_DEVICE_BOUNDS (site bit 18) in the device error word.
  */
 MOE_API moe_status_t moe_expert_ffn(const void* x_perm, const int32_t* offsets, int rows,
                             int H, int F, int E,
                             const void* w_gate, const void* w_up, const void* w_down,
-                            void* h, float* y, moe_stream_t stream);
+                            void* h, void* y, moe_stream_t stream);
 
 /* moe_expert_ffn with the activation chosen (moe_activation_t; an unknown
  * value returns MOE_ERR_INVALID_VALUE). */
 MOE_API moe_status_t moe_expert_ffn_ex(const void* x_perm, const int32_t* offsets, int rows,
                                int H, int F, int E,
                                const void* w_gate, const void* w_up, const void* w_down,
-                               int activation, void* h, float* y, moe_stream_t stream);
+                               int activation, void* h, void* y, moe_stream_t stream);
 
 /*
  * Fusion ablation, for measurement: the same grouped FFN with the gate and up
@@ -210,7 +217,7 @@ MOE_API moe_status_t moe_expert_ffn_ex(const void* x_perm, const int32_t* offset
 MOE_API moe_status_t moe_expert_ffn_unfused(const void* x_perm, const int32_t* offsets, int rows,
                                     int H, int F, int E,
                                     const void* w_gate, const void* w_up, const void* w_down,
-                                    int activation, void* g, void* u, void* h, float* y,
+                                    int activation, void* g, void* u, void* h, void* y,
                                     moe_stream_t stream);
 
 /*
@@ -229,22 +236,22 @@ MOE_API moe_status_t moe_expert_ffn_unfused(const void* x_perm, const int32_t* o
 MOE_API moe_status_t moe_expert_ffn_static(const void* x_perm, const int32_t* offsets, int rows,
                                    int H, int F, int E,
                                    const void* w_gate, const void* w_up, const void* w_down,
-                                   int block_m, void* h, float* y, moe_stream_t stream);
+                                   int block_m, void* h, void* y, moe_stream_t stream);
 
 /*
  * Weighted scatter-back ("The reading": scattered back with weights).
  * out[t] = sum_{j=0..k-1} topk_w[t,j] * y_perm[inv[t*k+j]]
  *          (+ s_t * y_shared[t]), summed in fp32 in that fixed order and
  * rounded once to bf16 (round to nearest even); deterministic.
- *   y_perm:       fp32 [T*k, H]
+ *   y_perm:       fp16 [T*k, H] (moe_expert_ffn's y)
  *   inv:          int32 [T*k]
  *   topk_w:       fp32 [T, k]
- *   y_shared:     fp32 [T, H] or NULL (no shared expert)
+ *   y_shared:     fp16 [T, H] or NULL (no shared expert)
  *   shared_scale: fp32 [T] or NULL (scale 1)
  *   out:          bf16 [T, H], fully overwritten
  */
-MOE_API moe_status_t moe_combine(const float* y_perm, const int32_t* inv, const float* topk_w,
-                         const float* y_shared, const float* shared_scale,
+MOE_API moe_status_t moe_combine(const void* y_perm, const int32_t* inv, const float* topk_w,
+                         const void* y_shared, const float* shared_scale,
                          int T, int H, int k, void* out, moe_stream_t stream);
 
 /*

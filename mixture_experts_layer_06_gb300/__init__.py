@@ -246,7 +246,7 @@ def moe_permute_noalloc(topk_idx, x, E, counts=None, offsets=None, perm=None, in
 
 def moe_expert_ffn(x_perm, offsets, w_gate, w_up, w_down, h=None, y=None, stream=None, activation="silu"):
     """Grouped gated FFN (SwiGLU, or GEGLU with activation="gelu").  offsets None =
-    one dense group (w_* given as [1,...] or 2-D).  Returns (h bf16 [rows,F], y fp32 [rows,H])."""
+    one dense group (w_* given as [1,...] or 2-D).  Returns (h bf16 [rows,F], y fp16 [rows,H])."""
     lib = load_library()
     rows, H = x_perm.shape
     if w_gate.dim() == 2:
@@ -254,14 +254,14 @@ def moe_expert_ffn(x_perm, offsets, w_gate, w_up, w_down, h=None, y=None, stream
     else:
         E, F = w_gate.shape[0], w_gate.shape[1]
     h = _out(h, (rows, F), torch.bfloat16, x_perm.device)
-    y = _out(y, (rows, H), torch.float32, x_perm.device)
+    y = _out(y, (rows, H), torch.float16, x_perm.device)
     if activation == "silu":
         st = lib.moe_expert_ffn(_ptr(x_perm), _ptr(offsets, torch.int32), rows, H, F, E, _ptr(w_gate), _ptr(w_up),
-                                _ptr(w_down), _ptr(h), _ptr(y, torch.float32), _stream(stream))
+                                _ptr(w_down), _ptr(h), _ptr(y, torch.float16), _stream(stream))
     else:
         st = lib.moe_expert_ffn_ex(_ptr(x_perm), _ptr(offsets, torch.int32), rows, H, F, E, _ptr(w_gate),
                                    _ptr(w_up), _ptr(w_down), ACTIVATIONS[activation], _ptr(h),
-                                   _ptr(y, torch.float32), _stream(stream))
+                                   _ptr(y, torch.float16), _stream(stream))
     _check(st, "moe_expert_ffn")
     return h, y
 
@@ -278,37 +278,37 @@ def moe_expert_ffn_unfused(x_perm, offsets, w_gate, w_up, w_down, activation="si
     g = torch.empty((rows, F), dtype=torch.bfloat16, device=x_perm.device)
     u = torch.empty_like(g)
     h = torch.empty_like(g)
-    y = torch.empty((rows, H), dtype=torch.float32, device=x_perm.device)
+    y = torch.empty((rows, H), dtype=torch.float16, device=x_perm.device)
     st = lib.moe_expert_ffn_unfused(_ptr(x_perm), _ptr(offsets, torch.int32), rows, H, F, E, _ptr(w_gate),
                                     _ptr(w_up), _ptr(w_down), ACTIVATIONS[activation], _ptr(g), _ptr(u), _ptr(h),
-                                    _ptr(y, torch.float32), _stream(stream))
+                                    _ptr(y, torch.float16), _stream(stream))
     _check(st, "moe_expert_ffn_unfused")
     return h, y, g, u
 
 
 def moe_expert_ffn_static(x_perm, offsets, w_gate, w_up, w_down, block_m=64, stream=None):
     """Schedule ablation: offsets read back to the host (a sync), fixed block_m
-    token tiles, one CTA per tile.  Returns (h bf16 [rows,F], y fp32 [rows,H])."""
+    token tiles, one CTA per tile.  Returns (h bf16 [rows,F], y fp16 [rows,H])."""
     lib = load_library()
     rows, H = x_perm.shape
     E, F = w_gate.shape[0], w_gate.shape[1]
     h = torch.empty((rows, F), dtype=torch.bfloat16, device=x_perm.device)
-    y = torch.empty((rows, H), dtype=torch.float32, device=x_perm.device)
+    y = torch.empty((rows, H), dtype=torch.float16, device=x_perm.device)
     st = lib.moe_expert_ffn_static(_ptr(x_perm), _ptr(offsets, torch.int32), rows, H, F, E, _ptr(w_gate),
-                                   _ptr(w_up), _ptr(w_down), int(block_m), _ptr(h), _ptr(y, torch.float32),
+                                   _ptr(w_up), _ptr(w_down), int(block_m), _ptr(h), _ptr(y, torch.float16),
                                    _stream(stream))
     _check(st, "moe_expert_ffn_static")
     return h, y
 
 
 def moe_combine(y_perm, inv, topk_w, y_shared=None, shared_scale=None, out=None, stream=None):
-    """Deterministic weighted scatter-back.  Returns out bf16 [T,H]."""
+    """Deterministic weighted scatter-back of fp16 expert outputs.  Returns out bf16 [T,H]."""
     lib = load_library()
     T, k = topk_w.shape
     H = y_perm.shape[1]
     out = _out(out, (T, H), torch.bfloat16, y_perm.device)
-    st = lib.moe_combine(_ptr(y_perm, torch.float32), _ptr(inv, torch.int32), _ptr(topk_w, torch.float32),
-                         _ptr(y_shared, torch.float32), _ptr(shared_scale, torch.float32), T, H, k, _ptr(out),
+    st = lib.moe_combine(_ptr(y_perm, torch.float16), _ptr(inv, torch.int32), _ptr(topk_w, torch.float32),
+                         _ptr(y_shared, torch.float16), _ptr(shared_scale, torch.float32), T, H, k, _ptr(out),
                          _stream(stream))
     _check(st, "moe_combine")
     return out

@@ -5,8 +5,8 @@
 // gathers its k expert rows (through inv) instead of the rows scattering into
 // the token, so no atomics are needed and the sum is taken in the fixed slot
 // order j = 0..k-1 (then the shared expert) in fp32, rounded once to bf16:
-// the result is bitwise deterministic.  One warp per (token, 256-column
-// chunk), 32-byte fp32 loads and 16-byte bf16 stores.
+// the result is bitwise deterministic.  The expert outputs arrive in fp16.
+// One warp per (token, 256-column chunk), 16-byte loads and stores.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -18,40 +18,45 @@ constexpr int kWarpsPerBlock = 8;
 constexpr int kMaxSlices = 8;  // K slices of the down projection (at most 8)
 constexpr long long kFewWarps = 4096;  // below this many warps the grid is latency-bound
 
-// Sum of the nslices partial-sum slices of 8 consecutive fp32 values, in
-// slice order.  MAXS > 0: all (<= MAXS) slices are loaded before the first
-// add, so their latencies overlap (for grids with few warps); MAXS == 0: one
-// slice after the other, in fewer registers (for grids with many warps,
-// where occupancy hides the latency).
+// 8 consecutive fp16 values (one 16-byte load) widened to fp32.
+__device__ __forceinline__ void widen8(const uint4 q, float (&v)[8]) {
+  const __half2* h = reinterpret_cast<const __half2*>(&q);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+
+// Sum of the nslices partial-sum slices of 8 consecutive fp16 values, in
+// slice order, in fp32.  MAXS > 0: all (<= MAXS) slices are loaded before the
+// first add, so their latencies overlap (for grids with few warps); MAXS ==
+// 0: one slice after the other, in fewer registers (for grids with many
+// warps, where occupancy hides the latency).
 template <int MAXS>
-__device__ __forceinline__ void load8(const float* p, int nslices, size_t stride, float (&v)[8]) {
+__device__ __forceinline__ void load8(const __half* p, int nslices, size_t stride, float (&v)[8]) {
   if constexpr (MAXS == 0) {
-    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    widen8(*reinterpret_cast<const uint4*>(p), v);
     for (int s = 1; s < nslices; ++s) {
-      const float4* q = reinterpret_cast<const float4*>(p + s * stride);
-      const float4 c = q[0], d = q[1];
-      v[0] += c.x; v[1] += c.y; v[2] += c.z; v[3] += c.w;
-      v[4] += d.x; v[5] += d.y; v[6] += d.z; v[7] += d.w;
+      float w[8];
+      widen8(*reinterpret_cast<const uint4*>(p + s * stride), w);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] += w[i];
     }
   } else {
-    float4 c[MAXS][2];
+    uint4 c[MAXS];
 #pragma unroll
-    for (int s = 0; s < MAXS; ++s) {
-      if (s < nslices) {
-        const float4* q = reinterpret_cast<const float4*>(p + s * stride);
-        c[s][0] = q[0];
-        c[s][1] = q[1];
-      }
-    }
-    v[0] = c[0][0].x; v[1] = c[0][0].y; v[2] = c[0][0].z; v[3] = c[0][0].w;
-    v[4] = c[0][1].x; v[5] = c[0][1].y; v[6] = c[0][1].z; v[7] = c[0][1].w;
+    for (int s = 0; s < MAXS; ++s)
+      if (s < nslices) c[s] = *reinterpret_cast<const uint4*>(p + s * stride);
+    widen8(c[0], v);
 #pragma unroll
     for (int s = 1; s < MAXS; ++s) {
       if (s < nslices) {
-        v[0] += c[s][0].x; v[1] += c[s][0].y; v[2] += c[s][0].z; v[3] += c[s][0].w;
-        v[4] += c[s][1].x; v[5] += c[s][1].y; v[6] += c[s][1].z; v[7] += c[s][1].w;
+        float w[8];
+        widen8(c[s], w);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] += w[i];
       }
     }
   }
@@ -60,8 +65,8 @@ __device__ __forceinline__ void load8(const float* p, int nslices, size_t stride
 // MR / MS: load8's MAXS for the routed rows / the shared expert's row.  G:
 // routed rows loaded before they are added.
 template <int MR, int MS, int G>
-__global__ void combine_kernel(const float* __restrict__ y_perm, const int32_t* __restrict__ inv,
-                               const float* __restrict__ topk_w, const float* __restrict__ y_shared,
+__global__ void combine_kernel(const __half* __restrict__ y_perm, const int32_t* __restrict__ inv,
+                               const float* __restrict__ topk_w, const __half* __restrict__ y_shared,
                                const float* __restrict__ shared_scale, int T, int H, int k,
                                __nv_bfloat16* __restrict__ out, int nslices, size_t stride, int nslices_sh,
                                size_t stride_sh) {
@@ -117,24 +122,26 @@ __global__ void combine_kernel(const float* __restrict__ y_perm, const int32_t* 
 
 }  // namespace
 
-cudaError_t launch_combine(const float* y_perm, const int32_t* inv, const float* topk_w, const float* y_shared,
+cudaError_t launch_combine(const void* y_perm, const int32_t* inv, const float* topk_w, const void* y_shared,
                            const float* shared_scale, int T, int H, int k, void* out, cudaStream_t stream,
                            int nslices, size_t slice_stride, int nslices_shared, size_t slice_stride_shared) {
   if (nslices < 1 || nslices > kMaxSlices || nslices_shared < 1 || nslices_shared > kMaxSlices)
     return cudaErrorInvalidValue;
   const int threads = kWarpsPerBlock * 32;
   const dim3 grid((T + kWarpsPerBlock - 1) / kWarpsPerBlock, (H + 255) / 256);
-  // Few warps (decode-sized batches): overlap the latencies inside each warp.
-  // Many warps: keep registers low so that occupancy hides them.
+  // Few warps (decode-sized batches): overlap the slice loads inside each
+  // warp.  Many warps: one slice after the other (fewer registers, occupancy
+  // hides the latency), four expert rows in flight per warp.
   const long long warps = static_cast<long long>(T) * grid.y;
-  void (*kernel)(const float*, const int32_t*, const float*, const float*, const float*, int, int, int,
-                 __nv_bfloat16*, int, size_t, int, size_t) = combine_kernel<0, 0, 1>;
+  void (*kernel)(const __half*, const int32_t*, const float*, const __half*, const float*, int, int, int,
+                 __nv_bfloat16*, int, size_t, int, size_t) = combine_kernel<0, 0, 4>;
   if (warps <= kFewWarps) {
     const bool rs = nslices > 1, ss = y_shared != nullptr && nslices_shared > 1;
     kernel = rs ? (ss ? combine_kernel<kMaxSlices, kMaxSlices, 1> : combine_kernel<kMaxSlices, 1, 1>)
                 : (ss ? combine_kernel<1, kMaxSlices, 4> : combine_kernel<1, 1, 4>);
   }
-  return launch_kernel(kernel, grid, dim3(threads), 0, stream, y_perm, inv, topk_w, y_shared, shared_scale, T, H, k,
+  return launch_kernel(kernel, grid, dim3(threads), 0, stream, static_cast<const __half*>(y_perm), inv, topk_w,
+                       static_cast<const __half*>(y_shared), shared_scale, T, H, k,
                        static_cast<__nv_bfloat16*>(out), nslices, slice_stride, nslices_shared,
                        slice_stride_shared);
 }

@@ -41,10 +41,7 @@ namespace {
 #ifndef MOE_EXACT_N
 #define MOE_EXACT_N 1
 #endif
-// Stages of L2 prefetch lookahead for the weight boxes (0: off).
-#ifndef MOE_PF_DIST
-#define MOE_PF_DIST 0
-#endif
+
 
 constexpr int kThreads = 192;
 constexpr int kMaxStages = 8;
@@ -84,7 +81,8 @@ struct GemmArgs {
   int stages;
   int kps;  // 64-wide K blocks per pipeline stage (one 3-D TMA box each)
   int bn_max;
-  int acc_cols;  // TMEM columns per accumulator slot (two slots): NSUB * bn_max
+  int acc_cols;  // TMEM columns per accumulator slot: NSUB * bn_max
+  int nslots;    // accumulator slots (2: the epilogue of a tile overlaps the next tile's MMAs)
   int tmem_cols;
   uint32_t* err;
 };
@@ -121,6 +119,18 @@ __device__ __forceinline__ void gated16(const uint32_t (&v)[32], const float (&p
 struct GemmMaps {
   SegMaps seg[2];
 };
+
+// Index of the token box a tile loads: the smallest of the segment's boxes
+// (bstep, 2 bstep, ...) that covers the tile's rows per CTA.  The producer
+// and the MMA issuer must agree on it: with several K blocks per stage, the
+// blocks of one box lie box-rows * 128 bytes apart in shared memory.
+#ifndef MOE_EXACT_BOX
+#define MOE_EXACT_BOX 1
+#endif
+__device__ __forceinline__ int box_index(const SegMaps& ms, int rows_per_cta) {
+  if (!MOE_EXACT_BOX) return ms.nb - 1;
+  return min(max((rows_per_cta + ms.bstep - 1) / ms.bstep - 1, 0), ms.nb - 1);
+}
 
 struct Tile {
   int s, g, mb, tb, a_row, b_row, valid, bn, kb0, kb1;
@@ -286,44 +296,9 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
       for (int sg = 0; sg < a.nseg; ++sg) {
         tma_prefetch_map(&maps.seg[sg].a0);
         if (SWIGLU && a.seg[sg].a_mode == kTwoMaps) tma_prefetch_map(&maps.seg[sg].a1);
-        tma_prefetch_map(&maps.seg[sg].b);
+        for (int i = 0; i < maps.seg[sg].nb; ++i) tma_prefetch_map(&maps.seg[sg].b[i]);
       }
       bool ok = true;
-#if MOE_PF_DIST > 0
-      // L2 prefetch of the weight boxes MOE_PF_DIST stages ahead of the loads,
-      // so that more weight bytes are in flight from DRAM than the shared
-      // memory ring holds (multi-K-block stages with the TMA box views only).
-      int pf_tile = first, pf_kb = 0;
-      Tile pt{};
-      bool pf_on = pf_tile < total;
-      if (pf_on) {
-        pt = decode_tile(a, sc, pf_tile);
-        pf_kb = pt.kb0;
-      }
-      auto pf_step = [&]() {
-        while (pf_on && pf_kb >= pt.kb1) {
-          pf_tile += stride;
-          pf_on = pf_tile < total;
-          if (pf_on) {
-            pt = decode_tile(a, sc, pf_tile);
-            pf_kb = pt.kb0;
-          }
-        }
-        if (!pf_on) return;
-        if (KPS > 1 && !(SWIGLU && a.seg[pt.s].a_mode == kTwoMaps)) {
-          const CUtensorMap* am = &maps.seg[pt.s].a0;
-          const int ar = pt.a_row + static_cast<int>(rank) * FEAT * NSUB;
-          for (int u = 0; u < NSUB; ++u) {
-            if (SWIGLU)
-              tma_prefetch_4d(am, 0, ar + u * kHalfRows, 0, pf_kb * KPS);
-            else
-              tma_prefetch_3d(am, 0, ar + u * kTileM, pf_kb * KPS);
-          }
-        }
-        ++pf_kb;
-      };
-      for (int i = 0; i < MOE_PF_DIST; ++i) pf_step();
-#endif
       for (int tile = first; tile < total && ok; tile += stride) {
         const Tile t = decode_tile(a, sc, tile);
         const SegMaps& ms = maps.seg[t.s];
@@ -331,7 +306,10 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
         const int n_tile = MOE_EXACT_N ? ((t.valid + 15) >> 4) << 4 : t.bn;
         const int a_row = t.a_row + static_cast<int>(rank) * FEAT * NSUB;
         const int b_row = t.b_row + static_cast<int>(rank) * (n_tile / BDIV);
-        const uint32_t bytes = BDIV * KPS * (NSUB * kATileBytes + (t.bn / BDIV) * kTileK * 2);
+        // the smallest token box that covers this CTA's n_tile / BDIV rows
+        const int bi = box_index(ms, n_tile / BDIV);
+        const CUtensorMap* mb = &ms.b[bi];
+        const uint32_t bytes = BDIV * KPS * (NSUB * kATileBytes + (bi + 1) * ms.bstep * kTileK * 2);
         for (int kb = t.kb0; kb < t.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
@@ -341,9 +319,6 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
           }
           uint8_t* st = smem + s * stage_bytes;
           uint8_t* sb = st + KPS * NSUB * kATileBytes;
-#if MOE_PF_DIST > 0
-          pf_step();
-#endif
           if (PAIR) {
             if (rank == 0) mbar_arrive_expect_tx(&full[s], bytes);
             const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
@@ -370,9 +345,9 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
               }
             }
             if (KPS == 1)
-              tma_load_2d_pair(sb, &ms.b, bar, kb * kTileK, b_row);
+              tma_load_2d_pair(sb, mb, bar, kb * kTileK, b_row);
             else
-              tma_load_3d_pair(sb, &ms.b, bar, 0, b_row, kb * KPS);
+              tma_load_3d_pair(sb, mb, bar, 0, b_row, kb * KPS);
           } else {
             mbar_arrive_expect_tx(&full[s], bytes);
             if (two_maps) {
@@ -398,9 +373,9 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
               }
             }
             if (KPS == 1)
-              tma_load_2d(sb, &ms.b, &full[s], kb * kTileK, b_row);
+              tma_load_2d(sb, mb, &full[s], kb * kTileK, b_row);
             else
-              tma_load_3d(sb, &ms.b, &full[s], 0, b_row, kb * KPS);
+              tma_load_3d(sb, mb, &full[s], 0, b_row, kb * KPS);
           }
         }
       }
@@ -421,13 +396,16 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
       bool ok = true;
       for (int tile = first; tile < total && ok; tile += stride, ++n) {
         const Tile t = decode_tile(a, sc, tile);
-        const int acc = n & 1;
-        const uint32_t aph = (n >> 1) & 1;
+        const int acc = a.nslots == 2 ? (n & 1) : 0;
+        const uint32_t aph = (a.nslots == 2 ? (n >> 1) : n) & 1;
         if (!mbar_wait(&tempty[acc], aph ^ 1, a.err, kSiteGemmMma)) break;
         tc_fence_after_sync();
         const uint32_t d = tmem_base + acc * a.acc_cols;
         const int n_tile = MOE_EXACT_N ? ((t.valid + 15) >> 4) << 4 : t.bn;
         const uint32_t idesc = idesc_bf16_f32(kTileM * BDIV, n_tile);
+        // consecutive K blocks of the token box lie box-rows * 128 bytes apart
+        const SegMaps& ms = maps.seg[t.s];
+        const uint32_t b_atom = (box_index(ms, n_tile / BDIV) + 1) * ms.bstep * kTileK * 2;
         for (int kb = t.kb0; kb < t.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
@@ -438,7 +416,6 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
           tc_fence_after_sync();
           const uint32_t a0 = smem_u32(smem + s * stage_bytes);
           const uint32_t bb = a0 + KPS * NSUB * kATileBytes;
-          const uint32_t b_atom = (t.bn / BDIV) * kTileK * 2;
           for (int j = 0; j < KPS; ++j) {
 #pragma unroll
             for (int kk = 0; kk < kTileK / 16; ++kk) {
@@ -479,8 +456,8 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
     int n = 0;
     for (int tile = first; tile < total && ok; tile += stride, ++n) {
       const Tile t = decode_tile(a, sc, tile);
-      const int acc = n & 1;
-      const uint32_t aph = (n >> 1) & 1;
+      const int acc = a.nslots == 2 ? (n & 1) : 0;
+      const uint32_t aph = (a.nslots == 2 ? (n >> 1) : n) & 1;
       if (!mbar_wait(&tfull[acc], aph, a.err, kSiteGemmEpilogue)) break;
       tc_fence_after_sync();
       const SegDev& sg = a.seg[t.s];
@@ -550,9 +527,11 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
             }
           }
         }
-      } else if constexpr (EPI == kEpiStoreBF16) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(sg.out);
-        __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(stg);
+      } else if constexpr (EPI == kEpiStoreBF16 || EPI == kEpiStoreF16) {
+        constexpr bool F16 = (EPI == kEpiStoreF16);
+        uint16_t* out = static_cast<uint16_t*>(sg.out) + t.out_off;
+        uint16_t* st = reinterpret_cast<uint16_t*>(stg);
+        float amax = 0.f;
         for (int u = 0; u < NSUB; ++u) {
           const int feat0 = t.mb * a.munit + static_cast<int>(rank) * FEAT * NSUB + u * FEAT + q * 32;
           for (int c0 = 0; c0 < ncols; c0 += 32) {
@@ -566,7 +545,15 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
             tmem_wait(g);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (j < nc) st[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(g[j]));
+              if (j < nc) {
+                const float v = __uint_as_float(g[j]);
+                if constexpr (F16) {
+                  amax = fmaxf(amax, fabsf(v));
+                  st[j * 32 + lane] = __half_as_ushort(__float2half_rn(v));
+                } else {
+                  st[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+                }
+              }
             __syncwarp();
             for (int w = lane; w < nc * 4; w += 32) {
               const int j = w >> 2, piece = w & 3;
@@ -578,6 +565,8 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
             __syncwarp();
           }
         }
+        // fp16 holds |v| <= 65504; anything larger (or NaN) is reported.
+        if (F16 && !(amax <= 65504.f)) raise_error(a.err, kErrBounds, kSiteOverflow);
       } else {
         float* out = static_cast<float*>(sg.out) + t.out_off;
         float* st = reinterpret_cast<float*>(stg);
@@ -678,6 +667,9 @@ constexpr int fixed_smem(int epi) {
   return 1024 + staging_bytes(epi) + static_cast<int>(sizeof(Sched)) + (2 * kMaxStages + 4 + 4) * 8 + 64;
 }
 
+// Epilogues whose partial sums may be cut into K slices.
+constexpr bool k_splittable(int epi) { return epi == kEpiStoreF32 || epi == kEpiStoreF16; }
+
 int bn_max_of(int num_segments, const GemmSegment* segs) {
   int m = 16;
   for (int s = 0; s < num_segments; ++s) m = m > segs[s].bn ? m : segs[s].bn;
@@ -719,6 +711,11 @@ int bn_max_of(int num_segments, const GemmSegment* segs) {
 #ifndef MOE_NSUB_SMALL
 #define MOE_NSUB_SMALL 2  // token tiles of 16..128 rows
 #endif
+// 256-row token tiles: sub-tiles per CTA.  Two fill TMEM with one tile's
+// accumulators (one slot: the epilogue no longer overlaps the next tile).
+#ifndef MOE_NSUB_LARGE
+#define MOE_NSUB_LARGE 1
+#endif
 #ifndef MOE_MIN_WAVE_FILL
 #define MOE_MIN_WAVE_FILL 0.9
 #endif
@@ -727,8 +724,8 @@ namespace {
 
 // Sub-tiles the plan starts from for token tiles of bn_max rows.
 int gemm_nsub(int bn_max) {
-  int n = bn_max >= 256 ? 1 : MOE_NSUB_SMALL;
-  while (n > 1 && 2 * n * bn_max > 512) n >>= 1;
+  int n = bn_max >= 256 ? MOE_NSUB_LARGE : MOE_NSUB_SMALL;
+  while (n > 1 && n * bn_max > 512) n >>= 1;
   return n;
 }
 
@@ -741,7 +738,7 @@ double wave_fill(GemmEpilogue epi, int num_segments, const GemmSegment* segs, in
     const long long active = g.offsets == nullptr ? 1 : (g.rows < g.groups ? g.rows : g.groups);
     if (active <= 0) continue;
     const long long per = (g.rows + active - 1) / active;
-    const int ks = (epi != kEpiStoreF32 || g.ksplit < 1) ? 1 : g.ksplit;
+    const int ks = (!k_splittable(epi) || g.ksplit < 1) ? 1 : g.ksplit;
     tiles += active * ((per + g.bn - 1) / g.bn) * (g.nout / munit) * ks;
   }
   if (tiles <= 0 || units <= 0) return 1.0;
@@ -775,7 +772,7 @@ GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment
   for (int cand = 2; cand <= MOE_KPS_MAX; cand <<= 1) {
     bool ok = (227 * 1024 - fixed_smem(epi)) / (cand * per_kb) >= min_stages;
     for (int s = 0; s < num_segments && ok; ++s) {
-      const int ks = (epi != kEpiStoreF32 || segs[s].ksplit < 1) ? 1 : segs[s].ksplit;
+      const int ks = (!k_splittable(epi) || segs[s].ksplit < 1) ? 1 : segs[s].ksplit;
       ok = segs[s].K % (kTileK * cand) == 0 && segs[s].K / (kTileK * cand) >= 2 * ks;
       if (epi == kEpiSwiGLU && segs[s].a_mode == kTwoMaps) ok = false;  // two 2-D boxes per stage
     }
@@ -794,14 +791,15 @@ cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSe
   long long upper = 0;
   for (int s = 0; s < num_segments; ++s) {
     const GemmSegment& g = segs[s];
-    const int ks = (epi != kEpiStoreF32 || g.ksplit < 1) ? 1 : g.ksplit;
+    const int ks = (!k_splittable(epi) || g.ksplit < 1) ? 1 : g.ksplit;
     a.seg[s] = SegDev{g.offsets, g.groups, g.rows, g.nout, g.K, g.bn, g.ldo, ks, g.a_mode, g.up_first, g.gelu,
                       g.slice_stride, g.out};
     a.bn_max = a.bn_max > g.bn ? a.bn_max : g.bn;
     upper += static_cast<long long>(g.nout / a.munit) * ((g.rows + g.bn - 1) / g.bn + g.groups) * ks;
   }
   a.acc_cols = plan.nsub * a.bn_max;
-  a.tmem_cols = static_cast<int>(pow2_at_least(static_cast<uint32_t>(2 * a.acc_cols)));
+  a.nslots = 2 * a.acc_cols <= 512 ? 2 : 1;
+  a.tmem_cols = static_cast<int>(pow2_at_least(static_cast<uint32_t>(a.nslots * a.acc_cols)));
   a.kps = plan.kps;
   const int stage_bytes =
       a.kps * (plan.nsub * kATileBytes + (plan.pair ? a.bn_max / 2 : a.bn_max) * kTileK * 2);
@@ -824,6 +822,10 @@ cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSe
   if (epi == kEpiStoreBF16) {
     if (plan.nsub == 2) return launch_epi<kEpiStoreBF16, 2>(a, maps, grid, smem, plan.pair, stream);
     return launch_epi<kEpiStoreBF16, 1>(a, maps, grid, smem, plan.pair, stream);
+  }
+  if (epi == kEpiStoreF16) {
+    if (plan.nsub == 2) return launch_epi<kEpiStoreF16, 2>(a, maps, grid, smem, plan.pair, stream);
+    return launch_epi<kEpiStoreF16, 1>(a, maps, grid, smem, plan.pair, stream);
   }
   if (plan.nsub == 2) return launch_epi<kEpiStoreF32, 2>(a, maps, grid, smem, plan.pair, stream);
   return launch_epi<kEpiStoreF32, 1>(a, maps, grid, smem, plan.pair, stream);

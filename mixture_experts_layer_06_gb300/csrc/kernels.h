@@ -37,6 +37,29 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   return e;
 }
 
+// launch_kernel for a grid of thread-block clusters of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                  unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = MOE_PDL;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  if (e == cudaSuccess) g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
+
 // Routing variant as the kernels see it.
 struct RouteSpec {
   int sigmoid;       // 0 softmax, 1 sigmoid
@@ -49,27 +72,36 @@ struct RouteSpec {
 };
 
 // Router launch plan: logit columns NE (E rounded up to 16, plus 16 when the
-// shared-expert gate vector rides along as one more B row), K slices and the
-// scratch (fp32 partial logits [ksplit][T][NE]) they need.  Shapes only.
+// shared-expert gate vector rides along as one more B row), and the K split:
+// a cluster of `cluster` CTAs per 128-token tile, each reducing kb_per_cta
+// 64-wide K blocks.  Shapes only.
 struct RouterPlan {
   bool fused_gate;
   int NE;
-  int ksplit;
-  int kb_per_split;
-  size_t scratch_bytes;
+  int cluster;
+  int kb_per_cta;
+  int m_tiles;
 };
 RouterPlan router_plan(int T, int H, int E, bool shared_gate);
 
-// Router GEMM (x [T,H] . [W_r; w_s]^T on the tensor cores, K-split) and the
-// per-token top-k.  map_x: box {64, 128}; map_wr: [E, H] box {64, E rounded up to 16};
-// map_ws: [1, H] box {64, 16} (used when the plan fuses the gate).
+// Router scoring + top-k in one launch (x [T,H] . [W_r; w_s]^T on the tensor
+// cores, partial logits of the cluster added over distributed shared memory,
+// then score, group limit and top-k per token), plus the separate shared-gate
+// kernel when the gate row does not fit.  map_x: box {64, 128}; map_wr: [E, H]
+// box {64, E rounded up to 16}; map_ws: [1, H] box {64, 16} (used when the
+// plan fuses the gate).
 cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_wr, const CUtensorMap* map_ws, int T,
                           int H, int E, int k, const RouteSpec& spec, const void* x, const void* w_shared_gate,
-                          int32_t* topk_idx, float* topk_w, float* shared_scale, void* scratch, uint32_t* err,
+                          int32_t* topk_idx, float* topk_w, float* shared_scale, uint32_t* err,
                           cudaStream_t stream);
+// Launches of launch_router for these shapes.
+int router_launches(int T, int H, int E, bool shared_gate);
 
-// Permutation: bitmap build, scan, gather (see permute.cu).
+// Permutation: bitmap build, scan, gather (see permute.cu); one launch for
+// small batches (permute_is_small), which then uses no scratch.
 size_t permute_scratch_bytes(int T, int E);
+bool permute_is_small(int T, int E);
+int permute_launches(int T, int E);
 cudaError_t launch_permute(const int32_t* topk_idx, const void* x, int T, int H, int E, int k, int32_t* counts,
                            int32_t* offsets, int32_t* perm, int32_t* inv, void* x_perm, void* scratch,
                            uint32_t* err, cudaStream_t stream);
@@ -91,9 +123,9 @@ struct GemmSegment {
   int nout;                // output features per group (multiple of 128)
   int K;                   // reduction length (multiple of 64)
   int bn;                  // token tile (16, 32, 64, 128, 256)
-  void* out;               // [rows, ldo] bf16 (SwiGLU) or fp32 (plain store)
+  void* out;               // [rows, ldo] bf16 (SwiGLU), fp32 / bf16 / fp16 (plain store)
   int ldo;
-  int ksplit = 1;          // plain store only: K cut into ksplit slices, slice s of
+  int ksplit = 1;          // fp32 / fp16 store only: K cut into ksplit slices, slice s of
                            // the partial sums goes to out + s * slice_stride
   size_t slice_stride = 0; // elements
   int a_mode = kStackedMap;  // SwiGLU only
@@ -105,7 +137,10 @@ struct GemmSegment {
 // bf16 (act = SiLU, or GELU with GemmSegment::gelu).  kEpiStoreF32: one
 // accumulator, fp32 out (K split allowed).  kEpiStoreBF16: one accumulator,
 // bf16 out (the unfused gate / up projections of the fusion ablation).
-enum GemmEpilogue { kEpiSwiGLU = 0, kEpiStoreF32 = 1, kEpiStoreBF16 = 2 };
+// kEpiStoreF16: one accumulator, fp16 out (K split allowed; the down
+// projection's expert outputs); a value beyond the fp16 range sets the device
+// error word.
+enum GemmEpilogue { kEpiSwiGLU = 0, kEpiStoreF32 = 1, kEpiStoreBF16 = 2, kEpiStoreF16 = 3 };
 
 // How the grouped GEMM will run these segments: as CTA pairs (tcgen05
 // cta_group::2; each CTA stages bn/2 token rows) or single CTAs, and with how
@@ -121,17 +156,23 @@ struct GemmPlan {
 GemmPlan grouped_gemm_plan(GemmEpilogue epi, int num_segments, const GemmSegment* segs, int num_sms,
                            bool static_grid = false);
 
-// TMA descriptors of one grouped-GEMM segment; b covers the [rows, K] token
-// rows with box {64 columns, bn (or bn/2) rows}, as a 3-D view {64, rows,
-// K/64} with box depth kps when kps > 1.
+// TMA descriptors of one grouped-GEMM segment.  The token rows [rows, K] are
+// read through nb maps of increasing box height: b[i] brings (i + 1) * bstep
+// rows (a 3-D view {64, rows, K/64} with box depth kps when kps > 1),
+// nb * bstep = bn (bn/2 for a CTA pair; bstep = 16, or bn/8 above 128 rows),
+// and every tile loads through the smallest box that covers its own rows, so
+// no tile fetches rows it does not use beyond the next multiple of bstep.
 //   Store:  a0 covers the [groups*nout, K] weights, box 128 rows.
 //   SwiGLU, kStackedMap: a0 is the view {K, groups*nout, 2} (kps == 1) or
 //           {64, groups*nout, 2, K/64} (kps > 1) of the gate and up weights
 //           (plane stride = the distance between them), box 64 rows x 2
 //           planes (x kps); one box per 64-feature sub-tile.
 //   SwiGLU, kTwoMaps: a0 / a1 cover the gate / up weights, box 64 rows.
+constexpr int kMaxBoxes = 8;
 struct SegMaps {
-  CUtensorMap a0, a1, b;
+  CUtensorMap a0, a1;
+  CUtensorMap b[kMaxBoxes];
+  int nb, bstep;
 };
 
 // Persistent grouped GEMM over one or two segments (seg_maps[s] for segment s).
@@ -150,10 +191,10 @@ uint32_t* device_error_word();
 // unfused gated activation of the fusion ablation).
 cudaError_t launch_gated_elementwise(const void* g, const void* u, void* h, size_t n, int gelu, cudaStream_t stream);
 
-// Deterministic weighted combine.  y_perm (and y_shared) may hold nslices
-// partial-sum slices slice_stride elements apart; they are added in slice
-// order before weighting.
-cudaError_t launch_combine(const float* y_perm, const int32_t* inv, const float* topk_w, const float* y_shared,
+// Deterministic weighted combine of fp16 expert outputs.  y_perm (and
+// y_shared) may hold nslices partial-sum slices slice_stride elements apart;
+// they are added in slice order (fp32) before weighting.
+cudaError_t launch_combine(const void* y_perm, const int32_t* inv, const float* topk_w, const void* y_shared,
                            const float* shared_scale, int T, int H, int k, void* out, cudaStream_t stream,
                            int nslices = 1, size_t slice_stride = 0, int nslices_shared = 1,
                            size_t slice_stride_shared = 0);

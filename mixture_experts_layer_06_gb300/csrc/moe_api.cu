@@ -121,6 +121,18 @@ bool make_gemm_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
   return kps == 1 ? make_map(m, base, rows, cols, box_rows) : make_map3d(m, base, rows, cols, box_rows, kps);
 }
 
+// The token-row maps of a grouped-GEMM segment: boxes of bstep, 2 bstep, ...,
+// max_rows rows (max_rows = the token tile per CTA: 16, 32, 64, 128 or 256;
+// bstep = 16, or max_rows / 8 above 128).
+bool make_token_maps(moe::SegMaps* m, const void* base, uint64_t rows, uint64_t cols, uint32_t max_rows, int kps) {
+  m->bstep = static_cast<int>(max_rows > 16u * moe::kMaxBoxes ? max_rows / moe::kMaxBoxes : 16u);
+  m->nb = static_cast<int>(max_rows) / m->bstep;
+  if (m->nb < 1 || m->nb > moe::kMaxBoxes || static_cast<int>(max_rows) != m->nb * m->bstep) return false;
+  for (int i = 0; i < m->nb; ++i)
+    if (!make_gemm_map(&m->b[i], base, rows, cols, static_cast<uint32_t>((i + 1) * m->bstep), kps)) return false;
+  return true;
+}
+
 // Stacked view of a SwiGLU segment's gate and up weights (both bf16
 // [rows, K] row-major): one more dimension of extent 2 whose stride is the
 // distance between the two tensors, lower address first, so that one box
@@ -234,19 +246,23 @@ int choose_bn(long long rows, int groups, int bn_max = 256) {
   return bn;
 }
 
-// Router scratch: fp32 partial logits of the K-split router GEMM.
+// Router scratch: none (the K-split partial logits are reduced on chip).
 size_t route_scratch(const moe_config_t& c, int T, int H, int E) {
-  return moe::router_plan(T, H, E, c.w_shared_gate != nullptr).scratch_bytes;
+  (void)c;
+  (void)T;
+  (void)H;
+  (void)E;
+  return 0;
 }
 
 // K-split of the down projection in moe_forward_ex.  When the routed rows
 // give too few output tiles to fill the GPU several times over (small T:
 // few active experts and one token tile each), K (= F) is cut into S <= 8
-// slices whose fp32 partial sums go to separate y slices; the combine adds
+// slices whose partial sums go to separate fp16 y slices; the combine adds
 // them in slice order, so the result stays deterministic.  S minimises a
 // two-term estimate: the weight bytes times the wave-quantisation loss of
 // tiles * S tiles on 152 SMs, plus the partial sums written and read back
-// (2 * S * T k * H * 4 bytes); a slice keeps >= 8 K blocks.  The shared
+// (2 * S * T k * H * 2 bytes); a slice keeps >= 8 K blocks.  The shared
 // expert's K (= F_shared) is cut so that its slices are no longer than the
 // routed ones.  Depends only on the shapes (not on the device), so that
 // moe_workspace_bytes() can size the slices.
@@ -272,7 +288,7 @@ Split choose_split(const moe_config_t& c, int T, int H, int F, int E, int k) {
     for (int S = 1; S <= 8 && kb / S >= 8; ++S) {
       const long long n = tiles * S;
       const double wave_loss = static_cast<double>((n + kSms - 1) / kSms * kSms) / static_cast<double>(n);
-      const double cost = weights * wave_loss + 2.0 * S * Tk * H * 4.0;
+      const double cost = weights * wave_loss + 2.0 * S * Tk * H * 2.0;
       if (S == 1 || cost < best * 0.99) {  // a larger S must win by more than 1 %
         best = cost;
         sp.routed = S;
@@ -321,24 +337,23 @@ Layout layout(const moe_config_t& c, int T, int H, int F, int E, int k) {
   L.x_perm = take(Tk * H * 2);
   L.h_perm = take(Tk * F * 2);
   const Split sp = choose_split(c, T, H, F, E, k);
-  L.y_perm = take(sp.routed * Tk * H * 4);
+  L.y_perm = take(sp.routed * Tk * H * 2);
   const size_t Fs = c.F_shared > 0 ? static_cast<size_t>(c.F_shared) : 0;
   L.h_shared = take(static_cast<size_t>(T) * Fs * 2);
-  L.y_shared = take(Fs ? sp.shared * static_cast<size_t>(T) * H * 4 : 0);
+  L.y_shared = take(Fs ? sp.shared * static_cast<size_t>(T) * H * 2 : 0);
   L.total = o;
   return L;
 }
 
 moe_status_t route_impl(DeviceState* d, const moe_config_t& c, const void* x, const void* w_router, int T, int H,
-                        int E, int k, int32_t* topk_idx, float* topk_w, float* shared_scale, void* scratch,
-                        cudaStream_t stream) {
+                        int E, int k, int32_t* topk_idx, float* topk_w, float* shared_scale, cudaStream_t stream) {
   CUtensorMap mx, mw, ms;
   if (!make_map(&mx, x, T, H, 128) || !make_map(&mw, w_router, E, H, (E + 15) / 16 * 16)) return MOE_ERR_CUDA;
   const bool gate = c.w_shared_gate != nullptr && shared_scale != nullptr;
   if (gate && !make_map(&ms, c.w_shared_gate, 1, H, 16)) return MOE_ERR_CUDA;
   const cudaError_t e = moe::launch_router(mx, mw, gate ? &ms : nullptr, T, H, E, k, route_spec(c), x,
                                            gate ? c.w_shared_gate : nullptr, topk_idx, topk_w,
-                                           gate ? shared_scale : nullptr, scratch, d->err, stream);
+                                           gate ? shared_scale : nullptr, d->err, stream);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -362,8 +377,8 @@ struct FfnOperands {
   int rows, groups, H, F;
   const void *w_gate, *w_up, *w_down;
   void* h;
-  float* y;
-  int ksplit = 1;  // down projection K slices (y holds ksplit slices of rows*H)
+  void* y;         // fp16 [rows, H] (ksplit slices of rows*H)
+  int ksplit = 1;  // down projection K slices
   int activation = MOE_ACT_SILU;
 };
 
@@ -398,7 +413,7 @@ moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStre
       } else if (!make_map(&maps[s].a0, o.w_gate, wrows, o.H, 64) || !make_map(&maps[s].a1, o.w_up, wrows, o.H, 64)) {
         return MOE_ERR_CUDA;
       }
-      if (!make_gemm_map(&maps[s].b, o.x_rows, o.rows, o.H, brows, plan.kps)) return MOE_ERR_CUDA;
+      if (!make_token_maps(&maps[s], o.x_rows, o.rows, o.H, brows, plan.kps)) return MOE_ERR_CUDA;
     }
     if (!replan) break;
   }
@@ -408,7 +423,7 @@ moe_status_t ffn_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStre
   return down_impl(d, nseg, ops, stream);
 }
 
-// The down projection: B = h [rows, F], A = down weights [groups*H, F], fp32 y
+// The down projection: B = h [rows, F], A = down weights [groups*H, F], fp16 y
 // (K-split slices when ops ask for them).
 moe_status_t down_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStream_t stream) {
   moe::SegMaps maps[2];
@@ -420,17 +435,17 @@ moe_status_t down_impl(DeviceState* d, int nseg, const FfnOperands* ops, cudaStr
     seg[s] = GemmSegment{o.offsets, o.groups, o.rows, o.H, o.F, bn, o.y, o.H, o.ksplit,
                          static_cast<size_t>(o.rows) * o.H};
   }
-  const moe::GemmPlan plan = moe::grouped_gemm_plan(moe::kEpiStoreF32, nseg, seg, d->num_sms);
+  const moe::GemmPlan plan = moe::grouped_gemm_plan(moe::kEpiStoreF16, nseg, seg, d->num_sms);
   for (int s = 0; s < nseg; ++s) {
     const FfnOperands& o = ops[s];
     const uint64_t wrows = static_cast<uint64_t>(o.groups) * o.H;
     const uint32_t brows = plan.pair ? seg[s].bn / 2 : seg[s].bn;
     if (!make_gemm_map(&maps[s].a0, o.w_down, wrows, o.F, 128, plan.kps) ||
-        !make_gemm_map(&maps[s].b, o.h, o.rows, o.F, brows, plan.kps))
+        !make_token_maps(&maps[s], o.h, o.rows, o.F, brows, plan.kps))
       return MOE_ERR_CUDA;
     maps[s].a1 = maps[s].a0;
   }
-  if (moe::launch_grouped_gemm(moe::kEpiStoreF32, nseg, seg, maps, d->num_sms, d->err, stream) != cudaSuccess)
+  if (moe::launch_grouped_gemm(moe::kEpiStoreF16, nseg, seg, maps, d->num_sms, d->err, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -444,7 +459,7 @@ moe_status_t ffn_unfused_impl(DeviceState* d, const FfnOperands& o, void* g, voi
   const uint64_t wrows = static_cast<uint64_t>(o.groups) * o.F;
   const uint32_t brows = plan.pair ? seg.bn / 2 : seg.bn;
   moe::SegMaps maps;
-  if (!make_gemm_map(&maps.b, o.x_rows, o.rows, o.H, brows, plan.kps)) return MOE_ERR_CUDA;
+  if (!make_token_maps(&maps, o.x_rows, o.rows, o.H, brows, plan.kps)) return MOE_ERR_CUDA;
   const void* w[2] = {o.w_gate, o.w_up};
   void* dst[2] = {g, u};
   for (int i = 0; i < 2; ++i) {
@@ -494,7 +509,7 @@ moe_status_t ffn_static_impl(DeviceState* d, const FfnOperands& o, int block_m, 
     } else if (!make_map(&maps.a0, o.w_gate, wrows, o.H, 64) || !make_map(&maps.a1, o.w_up, wrows, o.H, 64)) {
       return MOE_ERR_CUDA;
     }
-    if (!make_gemm_map(&maps.b, o.x_rows, o.rows, o.H, block_m, plan.kps)) return MOE_ERR_CUDA;
+    if (!make_token_maps(&maps, o.x_rows, o.rows, o.H, block_m, plan.kps)) return MOE_ERR_CUDA;
     break;
   }
   if (moe::launch_grouped_gemm(moe::kEpiSwiGLU, 1, &seg, &maps, d->num_sms, d->err, stream,
@@ -503,13 +518,13 @@ moe_status_t ffn_static_impl(DeviceState* d, const FfnOperands& o, int block_m, 
   // down: 128 output rows per CTA
   GemmSegment dseg = GemmSegment{o.offsets, o.groups, o.rows, o.H, o.F, block_m, o.y, o.H, 1,
                                  static_cast<size_t>(o.rows) * o.H};
-  const moe::GemmPlan dplan = moe::grouped_gemm_plan(moe::kEpiStoreF32, 1, &dseg, d->num_sms, true);
+  const moe::GemmPlan dplan = moe::grouped_gemm_plan(moe::kEpiStoreF16, 1, &dseg, d->num_sms, true);
   moe::SegMaps dmaps;
   if (!make_gemm_map(&dmaps.a0, o.w_down, static_cast<uint64_t>(o.groups) * o.H, o.F, 128, dplan.kps) ||
-      !make_gemm_map(&dmaps.b, o.h, o.rows, o.F, block_m, dplan.kps))
+      !make_token_maps(&dmaps, o.h, o.rows, o.F, block_m, dplan.kps))
     return MOE_ERR_CUDA;
   dmaps.a1 = dmaps.a0;
-  if (moe::launch_grouped_gemm(moe::kEpiStoreF32, 1, &dseg, &dmaps, d->num_sms, d->err, stream,
+  if (moe::launch_grouped_gemm(moe::kEpiStoreF16, 1, &dseg, &dmaps, d->num_sms, d->err, stream,
                                token_tiles * (o.H / 128)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
@@ -518,9 +533,8 @@ moe_status_t ffn_static_impl(DeviceState* d, const FfnOperands& o, int block_m, 
 // Kernels moe_forward_ex launches for these shapes (its launch sequence below).
 int forward_launches(const moe_config_t& c, int T, int H, int E) {
   if (T == 0) return 0;
-  const moe::RouterPlan rp = moe::router_plan(T, H, E, c.w_shared_gate != nullptr);
-  const int route = 2 + ((c.w_shared_gate != nullptr && !rp.fused_gate) ? 1 : 0);
-  const int permute = 3;
+  const int route = moe::router_launches(T, H, E, c.w_shared_gate != nullptr);
+  const int permute = moe::permute_launches(T, E);
   const int ffn = 2;
   const int combine = 1;
   return route + permute + ffn + combine;
@@ -603,11 +617,12 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x, const void* w_rou
   if (c.w_shared_gate && !shared_scale) return MOE_ERR_INVALID_VALUE;
   if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_VALUE;
   if (T == 0) return MOE_OK;
-  if (!scratch || !aligned16(scratch)) return MOE_ERR_INVALID_VALUE;
-  if (scratch_bytes < route_scratch(c, T, H, E)) return MOE_ERR_WORKSPACE;
+  const size_t need = route_scratch(c, T, H, E);
+  if (need > 0 && (!scratch || !aligned16(scratch))) return MOE_ERR_INVALID_VALUE;
+  if (scratch_bytes < need) return MOE_ERR_WORKSPACE;
   DeviceState* d = nullptr;
   if ((st = device_state(&d)) != MOE_OK) return st;
-  return route_impl(d, c, x, w_router, T, H, E, k, topk_idx, topk_w, shared_scale, scratch,
+  return route_impl(d, c, x, w_router, T, H, E, k, topk_idx, topk_w, shared_scale,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -632,14 +647,14 @@ moe_status_t moe_permute(const int32_t* topk_idx, const void* x, int T, int H, i
 }
 
 moe_status_t moe_expert_ffn(const void* x_perm, const int32_t* offsets, int rows, int H, int F, int E,
-                            const void* w_gate, const void* w_up, const void* w_down, void* h, float* y,
+                            const void* w_gate, const void* w_up, const void* w_down, void* h, void* y,
                             moe_stream_t stream) {
   return moe_expert_ffn_ex(x_perm, offsets, rows, H, F, E, w_gate, w_up, w_down, MOE_ACT_SILU, h, y, stream);
 }
 
 moe_status_t moe_expert_ffn_static(const void* x_perm, const int32_t* offsets, int rows, int H, int F, int E,
                                    const void* w_gate, const void* w_up, const void* w_down, int block_m, void* h,
-                                   float* y, moe_stream_t stream) {
+                                   void* y, moe_stream_t stream) {
   if (block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128 && block_m != 256)
     return MOE_ERR_INVALID_VALUE;
   moe_status_t st = check_dims(rows, H, F, E, 1);
@@ -657,7 +672,7 @@ moe_status_t moe_expert_ffn_static(const void* x_perm, const int32_t* offsets, i
 
 moe_status_t moe_expert_ffn_unfused(const void* x_perm, const int32_t* offsets, int rows, int H, int F, int E,
                                     const void* w_gate, const void* w_up, const void* w_down, int activation,
-                                    void* g, void* u, void* h, float* y, moe_stream_t stream) {
+                                    void* g, void* u, void* h, void* y, moe_stream_t stream) {
   if (activation != MOE_ACT_SILU && activation != MOE_ACT_GELU) return MOE_ERR_INVALID_VALUE;
   moe_status_t st = check_dims(rows, H, F, E, 1);
   if (st != MOE_OK) return st;
@@ -676,7 +691,7 @@ moe_status_t moe_expert_ffn_unfused(const void* x_perm, const int32_t* offsets, 
 
 moe_status_t moe_expert_ffn_ex(const void* x_perm, const int32_t* offsets, int rows, int H, int F, int E,
                                const void* w_gate, const void* w_up, const void* w_down, int activation, void* h,
-                               float* y, moe_stream_t stream) {
+                               void* y, moe_stream_t stream) {
   if (activation != MOE_ACT_SILU && activation != MOE_ACT_GELU) return MOE_ERR_INVALID_VALUE;
   moe_status_t st = check_dims(rows, H, F, E, 1);
   if (st != MOE_OK) return st;
@@ -693,7 +708,7 @@ moe_status_t moe_expert_ffn_ex(const void* x_perm, const int32_t* offsets, int r
   return ffn_impl(d, 1, &o, reinterpret_cast<cudaStream_t>(stream));
 }
 
-moe_status_t moe_combine(const float* y_perm, const int32_t* inv, const float* topk_w, const float* y_shared,
+moe_status_t moe_combine(const void* y_perm, const int32_t* inv, const float* topk_w, const void* y_shared,
                          const float* shared_scale, int T, int H, int k, void* out, moe_stream_t stream) {
   if (T < 0 || H <= 0 || k <= 0 || k > 16) return MOE_ERR_INVALID_VALUE;
   if (H % 128 != 0) return MOE_ERR_UNSUPPORTED;
@@ -745,8 +760,7 @@ moe_status_t moe_forward_ex(const moe_config_t* cfg, const void* x, const void* 
   const int Tk = T * k;
 
   trace(0, s);
-  if ((st = route_impl(d, c, x, w_router, T, H, E, k, topk_idx, topk_w, shared_scale, at(L.route_scratch), s)) !=
-      MOE_OK)
+  if ((st = route_impl(d, c, x, w_router, T, H, E, k, topk_idx, topk_w, shared_scale, s)) != MOE_OK)
     return st;
   trace(1, s);
   if ((st = permute_impl(d, topk_idx, x, T, H, E, k, static_cast<int32_t*>(at(L.counts)), offsets,
@@ -755,11 +769,11 @@ moe_status_t moe_forward_ex(const moe_config_t* cfg, const void* x, const void* 
   const Split sp = choose_split(c, T, H, F, E, k);
   FfnOperands ops[2];
   ops[0] = FfnOperands{at(L.x_perm), offsets, Tk, E, H, F, w_gate, w_up, w_down, at(L.h_perm),
-                       static_cast<float*>(at(L.y_perm)), sp.routed, c.activation};
+                       at(L.y_perm), sp.routed, c.activation};
   int nseg = 1;
-  float* y_shared = nullptr;
+  void* y_shared = nullptr;
   if (c.F_shared > 0) {
-    y_shared = static_cast<float*>(at(L.y_shared));
+    y_shared = at(L.y_shared);
     ops[1] = FfnOperands{x, nullptr, T, 1, H, c.F_shared, c.ws_gate, c.ws_up, c.ws_down, at(L.h_shared), y_shared,
                          sp.shared, c.activation};
     nseg = 2;
@@ -767,7 +781,7 @@ moe_status_t moe_forward_ex(const moe_config_t* cfg, const void* x, const void* 
   trace(2, s);
   if ((st = ffn_impl(d, nseg, ops, s, true)) != MOE_OK) return st;
   trace(4, s);
-  st = cuda_status(moe::launch_combine(static_cast<float*>(at(L.y_perm)), inv, topk_w, y_shared, shared_scale, T,
+  st = cuda_status(moe::launch_combine(at(L.y_perm), inv, topk_w, y_shared, shared_scale, T,
                                        H, k, out, s, sp.routed, static_cast<size_t>(Tk) * H, sp.shared,
                                        static_cast<size_t>(T) * H));
   trace(5, s);

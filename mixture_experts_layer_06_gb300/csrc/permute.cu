@@ -158,7 +158,107 @@ __global__ void gather_kernel(const int32_t* __restrict__ idx, const uint4* __re
   }
 }
 
+// Small batches (T <= kSmallT): the whole permutation in one launch.  Every
+// CTA builds the token bitmaps, the counts, the exclusive scan and the row
+// bases of all T tokens in its own shared memory (at most kSmallT / 32 * E
+// words each: cheap to repeat), then copies its share of the x_perm rows;
+// CTA 0 also writes counts, offsets, perm and inv.
+// Same arithmetic, same results as the three-launch form.
+constexpr int kSmallT = 512;
+constexpr int kSmallThreads = 256;
+
+__global__ void __launch_bounds__(kSmallThreads)
+    permute_small_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int T, int H8, int E, int k,
+                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                         int32_t* __restrict__ inv, uint4* __restrict__ x_perm, uint32_t* err) {
+  __shared__ uint32_t bm[kSmallT / 32][256];
+  __shared__ uint32_t rowbase[kSmallT / 32][256];
+  __shared__ int32_t off_s[257];
+  __shared__ int32_t warp_tot[8];
+  pdl_trigger();
+  pdl_wait();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int W = (T + 31) / 32;
+  for (int i = tid; i < W * 256; i += kSmallThreads) bm[i / 256][i % 256] = 0;
+  __syncthreads();
+  // bitmaps: warp w' handles token words w', w' + 8, ...
+  for (int w = warp; w < W; w += kSmallThreads / 32) {
+    const int t = w * 32 + lane;
+    for (int j = 0; j < k; ++j) {
+      int e = -1;
+      if (t < T) {
+        e = idx[static_cast<size_t>(t) * k + j];
+        if (e < 0 || e >= E) {
+          if (blockIdx.x == 0) raise_error(err, kErrBounds, kSitePermuteIndex);
+          e = -1;
+        }
+      }
+      const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
+      if (e >= 0 && lane == __ffs(peers) - 1) {
+        if ((bm[w][e] & peers) && blockIdx.x == 0) raise_error(err, kErrBounds, kSitePermuteIndex);
+        bm[w][e] |= peers;
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  // counts and the exclusive scan (thread e < E <= 256)
+  int32_t cnt = 0;
+  if (tid < E)
+    for (int w = 0; w < W; ++w) cnt += __popc(bm[w][tid]);
+  int32_t incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int32_t base = 0;
+  for (int w = 0; w < warp; ++w) base += warp_tot[w];
+  if (tid < E) {
+    off_s[tid] = base + incl - cnt;
+    uint32_t run = static_cast<uint32_t>(base + incl - cnt);
+    for (int w = 0; w < W; ++w) {
+      rowbase[w][tid] = run;
+      run += __popc(bm[w][tid]);
+    }
+    if (blockIdx.x == 0) counts[tid] = cnt;
+  }
+  if (tid == E - 1) off_s[E] = base + incl;
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int e = tid; e <= E; e += kSmallThreads) offsets[e] = off_s[e];
+  // grouped row of copy q = t * k + j (-1: dropped id)
+  const int rows = T * k;
+  auto row_of = [&](int q) {
+    const int t = q / k;
+    const int e = idx[q];
+    if (e < 0 || e >= E) return -1;
+    const int r = static_cast<int>(rowbase[t >> 5][e] + __popc(bm[t >> 5][e] & ((1u << (t & 31)) - 1u)));
+    return r < rows ? r : -1;
+  };
+  if (blockIdx.x == 0)
+    for (int q = tid; q < rows; q += kSmallThreads) {
+      const int r = row_of(q);
+      if (r >= 0) perm[r] = q;
+      inv[q] = r;
+    }
+  // x_perm: CTA b copies the rows of copies b, b + gridDim.x, ... (16-byte pieces)
+  for (int q = blockIdx.x; q < rows; q += gridDim.x) {
+    const int r = row_of(q);  // the same for every thread of the CTA
+    if (r < 0) continue;
+    const uint4* src = x + static_cast<size_t>(q / k) * H8;
+    uint4* dst = x_perm + static_cast<size_t>(r) * H8;
+    for (int v = tid; v < H8; v += kSmallThreads) dst[v] = src[v];
+  }
+}
+
 }  // namespace
+
+bool permute_is_small(int T, int E) { return T <= kSmallT && E <= 256; }
+
+int permute_launches(int T, int E) { return T == 0 ? 0 : permute_is_small(T, E) ? 1 : 3; }
 
 size_t permute_scratch_bytes(int T, int E) {
   const size_t W = (static_cast<size_t>(T) + 31) / 32;
@@ -168,6 +268,14 @@ size_t permute_scratch_bytes(int T, int E) {
 cudaError_t launch_permute(const int32_t* topk_idx, const void* x, int T, int H, int E, int k, int32_t* counts,
                            int32_t* offsets, int32_t* perm, int32_t* inv, void* x_perm, void* scratch,
                            uint32_t* err, cudaStream_t stream) {
+  if (permute_is_small(T, E)) {
+    long long g = static_cast<long long>(T) * k;  // one CTA per copied row, at most one wave
+    if (g > 148) g = 148;
+    if (g < 1) g = 1;
+    return launch_kernel(permute_small_kernel, dim3(static_cast<unsigned>(g)), dim3(kSmallThreads), 0, stream,
+                         topk_idx, static_cast<const uint4*>(x), T, H / 8, E, k, counts, offsets, perm, inv,
+                         static_cast<uint4*>(x_perm), err);
+  }
   const int W = (T + 31) / 32;
   uint32_t* bitmap = static_cast<uint32_t*>(scratch);
   uint32_t* rowbase = bitmap + static_cast<size_t>(W) * E;

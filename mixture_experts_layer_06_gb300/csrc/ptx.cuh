@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace moe {
 
@@ -24,6 +25,7 @@ enum ErrSite : uint32_t {
   kSitePermuteIndex = 7,
   kSiteTeardown = 8,
   kSiteSelfTest = 9,
+  kSiteOverflow = 10,  // an expert output beyond the fp16 range
 };
 
 __device__ __forceinline__ void raise_error(uint32_t* err, uint32_t kind, uint32_t site) {
@@ -137,19 +139,6 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* m
       ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z),
       "r"(w)
       : "memory");
-}
-
-// L2 prefetch of a tiled box (no shared-memory destination, no completion).
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
-               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int x, int y, int z, int w) {
-  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
-               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w)
-               : "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05

@@ -1,20 +1,22 @@
-// Router scoring + top-k selection.
+// Router scoring + top-k selection, one launch.
 //
 // "Cross-Platform Fused MoE Dispatch in Triton" (review page), "The reading":
 // every token is first scored by the router; "Assumptions & free parameters":
 // the standard softmax/sigmoid router with top-k selection.
 //
-// Two launches:
-//  1. router_gemm_kernel: logits = x . [W_r; w_s]^T on the 5th-generation
-//     tensor cores (tcgen05.mma, operands staged by TMA, fp32 accumulator in
-//     TMEM).  The grid is (token tiles of 128) x (K slices), so that even a
-//     single token spreads the W_r stream over many SMs; each CTA writes its
-//     fp32 partial logits to a slice of the scratch.  With a sigmoid-gated
-//     shared expert the gate vector w_s rides along as one more B row.
-//  2. router_topk_kernel: one warp per token adds the K-slice partials in
-//     slice order, applies the logit bias and the score function, optional
-//     group limiting, and picks the k best experts by warp-wide arg-max
-//     rounds (ties to the lower expert index).  Deterministic.
+// router_kernel: a cluster of C CTAs per tile of 128 tokens.  CTA r of the
+// cluster computes the partial logits x . [W_r; w_s]^T over its share of the
+// K = H columns on the 5th-generation tensor cores (tcgen05.mma, operands
+// staged by TMA, fp32 accumulator in TMEM).  CTA r owns tokens
+// [r*128/C, (r+1)*128/C) of the tile: every CTA stores its partial logits of
+// a token into the owner's shared memory (distributed shared memory stores,
+// slot = source rank, column-major so that a warp's stores are contiguous),
+// the owner adds the C partials in rank order, and a team of 8 lanes per
+// owned token applies the logit bias and the score function, the optional
+// group limit, and picks the k best experts (ties to the lower expert
+// index).  Deterministic; no partial logits go to global memory.
+// With a sigmoid-gated shared expert the gate vector w_s rides along as one
+// more B row (its logit column gives the gate), else shared_gate_kernel.
 #include <cfloat>
 #include <climits>
 
@@ -24,44 +26,245 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 192;  // warp 0: TMA, warp 1: MMA + TMEM owner, warps 2-5: epilogue
+constexpr int kThreads = 192;  // warp 0: TMA, warp 1: MMA + TMEM owner, warps 2-5: TMEM -> shared memory
 constexpr int kMaxStages = 8;
-constexpr int kTileM = 128;    // tokens per CTA
+constexpr int kMaxCluster = 8;
+constexpr int kTileM = 128;    // tokens per cluster
 constexpr int kTileK = 64;     // bf16 elements per 128-byte swizzled row
 constexpr int kATileBytes = kTileM * kTileK * 2;
 constexpr int kBoxBytes = 16 * kTileK * 2;  // one 16-row box of B rows
-constexpr int kJMax = 8;                    // logit columns per lane in the top-k kernel (<= 256 columns)
 
-struct GemmArgs {
-  int T, H, NE, n_wr_boxes, gate_box, stages, tmem_cols, kb_per_split;
-  float* partial;  // [ksplit][T][NE]
+struct RouterArgs {
+  int T, H, E, k, NE, n_wr_boxes, gate_box, gate_col, stages, tmem_cols, kb_per_cta;
+  RouteSpec spec;
+  int32_t* topk_idx;
+  float* topk_w;
+  float* shared_scale;
   uint32_t* err;
 };
 
+// The partial-logit slots R[C][NE][ld] (column-major per source slot: the
+// tokens of one logit column are contiguous, so a warp's stores of a column
+// are one contiguous run) with ld = 128/C + 4: a multiple of 4 times an odd
+// number modulo 32 banks, so that the 8-lane teams of the selection, reading
+// experts tl, tl + 8, ... of 4 tokens, touch 32 distinct banks.  Then room for
+// the logit bias of up to 256 experts.
+__host__ __device__ constexpr int logit_ld(int C) { return kTileM / C + 4; }
+__host__ __device__ constexpr int logit_buffer_bytes(int NE, int C) { return C * NE * logit_ld(C) * 4 + 256 * 4; }
+
+constexpr int kTeam = 8;  // lanes that select the experts of one token
+
+__device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
+  return v1 > v2 || (v1 == v2 && i1 < i2);
+}
+
+// The k best experts of one token by a team of 8 lanes (tl = lane within the
+// team), from its summed logits L[e * ld] and the logit bias (both in shared
+// memory; bias may be null).  Lane tl looks at experts tl, tl + 8, ...  The
+// score functions are monotone, so experts (and a group's top scores) are
+// ranked by logit; scores are evaluated only where a value is needed.  Ties
+// go to the lower expert (group) index.  Every lane of the warp calls this
+// (the shuffles span the warp); only `active` teams write.  KMAX >= k.
+template <int KMAX>
+__device__ void select_team(const float* L, int ld, const float* bias, const RouterArgs& a, int t, int tl,
+                            bool active) {
+  const int E = a.E, k = a.k;
+  const bool sigmoid = a.spec.sigmoid != 0;
+  auto logit = [&](int e) { return bias != nullptr ? L[e * ld] + bias[e] : L[e * ld]; };
+  if (active && tl == 0 && a.gate_col >= 0) a.shared_scale[t] = 1.f / (1.f + __expf(-L[a.gate_col * ld]));
+  const int ng = a.spec.n_group > 1 ? a.spec.n_group : 1;
+  const int gsize = E / ng;
+
+  // Softmax normaliser over all E logits, when a softmax score is used
+  // un-renormalised or inside a group score.
+  float mx = -INFINITY, inv_se = 1.f;
+  if (!sigmoid && (!a.spec.renormalize || ng > 1)) {
+    for (int e = tl; e < E; e += kTeam) mx = fmaxf(mx, logit(e));
+#pragma unroll
+    for (int o = kTeam / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    float se = 0.f;
+    for (int e = tl; e < E; e += kTeam) se += __expf(logit(e) - mx);
+#pragma unroll
+    for (int o = kTeam / 2; o > 0; o >>= 1) se += __shfl_xor_sync(0xFFFFFFFFu, se, o);
+    inv_se = 1.f / se;
+  }
+  auto score = [&](float v) { return sigmoid ? 1.f / (1.f + __expf(-v)) : __expf(v - mx) * inv_se; };
+
+  // Group limit: group score = sum of the scores of its group_topn best
+  // logits; the topk_group best groups are kept.  Lane tl holds the scores of
+  // groups tl and tl + 8 (n_group <= 16).
+  uint32_t kept = 0xFFFFFFFFu;
+  if (ng > 1) {
+    float gs_lo = -INFINITY, gs_hi = -INFINITY;
+    for (int g = 0; g < ng; ++g) {
+      float c[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // this lane's best four, descending
+      for (int e = g * gsize + tl; e < (g + 1) * gsize; e += kTeam) {
+        float v = logit(e), m;
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+          m = fminf(c[j], v);
+          c[j] = fmaxf(c[j], v);
+          v = m;
+        }
+        c[3] = fmaxf(c[3], v);
+      }
+      // team merge: the best four of two descending lists (bitonic half
+      // cleaner, then a 4-element bitonic sort)
+#pragma unroll
+      for (int o = kTeam / 2; o > 0; o >>= 1) {
+        float d[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) d[j] = fmaxf(c[j], __shfl_xor_sync(0xFFFFFFFFu, c[3 - j], o));
+        float x;
+        x = fmaxf(d[0], d[2]); d[2] = fminf(d[0], d[2]); d[0] = x;
+        x = fmaxf(d[1], d[3]); d[3] = fminf(d[1], d[3]); d[1] = x;
+        x = fmaxf(d[0], d[1]); d[1] = fminf(d[0], d[1]); d[0] = x;
+        x = fmaxf(d[2], d[3]); d[3] = fminf(d[2], d[3]); d[2] = x;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) c[j] = d[j];
+      }
+      const int n = a.spec.group_topn;
+      const float sg = score(c[0]) + (n > 1 ? score(c[1]) : 0.f) + (n > 2 ? score(c[2]) : 0.f) +
+                       (n > 3 ? score(c[3]) : 0.f);
+      if (g == tl) gs_lo = sg;
+      if (g == tl + kTeam) gs_hi = sg;
+    }
+    kept = 0;
+    for (int r = 0; r < a.spec.topk_group; ++r) {
+      // the best group not kept yet: this lane's candidate, then the team's
+      const bool lo_ok = tl < ng && !((kept >> tl) & 1u), hi_ok = tl + kTeam < ng && !((kept >> (tl + kTeam)) & 1u);
+      float v = lo_ok ? gs_lo : -INFINITY;
+      int i = lo_ok ? tl : INT_MAX;
+      if (hi_ok && (i == INT_MAX || gs_hi > v)) {
+        v = gs_hi;
+        i = tl + kTeam;
+      }
+#pragma unroll
+      for (int o = kTeam / 2; o > 0; o >>= 1) {
+        const float v2 = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        const int i2 = __shfl_xor_sync(0xFFFFFFFFu, i, o);
+        if (better(v2, i2, v, i)) {
+          v = v2;
+          i = i2;
+        }
+      }
+      if (i != INT_MAX) kept |= 1u << i;
+    }
+  }
+
+  // This lane's best KMAX candidates by logit, descending (lower id first
+  // among equals: the experts are scanned in increasing order).
+  float bv[KMAX];
+  int bi[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    bv[j] = -INFINITY;
+    bi[j] = INT_MAX;
+  }
+  int g = 0, gend = gsize;
+  for (int e = tl; e < E; e += kTeam) {
+    while (e >= gend) {
+      ++g;
+      gend += gsize;
+    }
+    if (!((kept >> g) & 1u)) continue;
+    const float v = logit(e);
+    if (v > bv[KMAX - 1] || bi[KMAX - 1] == INT_MAX) {
+      bv[KMAX - 1] = v;
+      bi[KMAX - 1] = e;
+#pragma unroll
+      for (int j = KMAX - 1; j > 0; --j) {
+        if (bv[j] > bv[j - 1] || (bi[j - 1] == INT_MAX && bi[j] != INT_MAX)) {
+          const float tv = bv[j];
+          bv[j] = bv[j - 1];
+          bv[j - 1] = tv;
+          const int ti = bi[j];
+          bi[j] = bi[j - 1];
+          bi[j - 1] = ti;
+        }
+      }
+    }
+  }
+
+  // k rounds: the team's best head wins the round; its lane pops it.  The
+  // weights are the scores of the k winners, renormalised over them when
+  // asked (a renormalised softmax needs only the winners' logits: its
+  // denominator cancels), times the routed scaling factor.
+  const bool renorm_softmax = !sigmoid && a.spec.renormalize && ng == 1;
+  float v0 = 0.f, sum = 0.f, s_lo = 0.f, s_hi = 0.f;
+  int i_lo = -1, i_hi = -1;
+  for (int r = 0; r < k; ++r) {
+    float v = bv[0];
+    int i = bi[0];
+#pragma unroll
+    for (int o = kTeam / 2; o > 0; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+      const int i2 = __shfl_xor_sync(0xFFFFFFFFu, i, o);
+      if (better(v2, i2, v, i)) {
+        v = v2;
+        i = i2;
+      }
+    }
+    if (i == bi[0] && i != INT_MAX) {  // this lane's head won: pop it
+#pragma unroll
+      for (int j = 0; j < KMAX - 1; ++j) {
+        bv[j] = bv[j + 1];
+        bi[j] = bi[j + 1];
+      }
+      bv[KMAX - 1] = -INFINITY;
+      bi[KMAX - 1] = INT_MAX;
+    }
+    if (r == 0) v0 = v;
+    const float sc = renorm_softmax ? __expf(v - v0) : score(v);
+    sum += sc;
+    if (r == tl) {
+      s_lo = sc;
+      i_lo = i;
+    } else if (r == tl + kTeam) {
+      s_hi = sc;
+      i_hi = i;
+    }
+  }
+  const float scale = a.spec.renormalize ? a.spec.route_scale / sum : a.spec.route_scale;
+  if (active) {
+    if (tl < k) {
+      a.topk_idx[static_cast<size_t>(t) * k + tl] = i_lo;
+      a.topk_w[static_cast<size_t>(t) * k + tl] = s_lo * scale;
+    }
+    if (tl + kTeam < k) {
+      a.topk_idx[static_cast<size_t>(t) * k + tl + kTeam] = i_hi;
+      a.topk_w[static_cast<size_t>(t) * k + tl + kTeam] = s_hi * scale;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    router_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_wr,
-                       const __grid_constant__ CUtensorMap map_ws, const GemmArgs a) {
+    router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_wr,
+                  const __grid_constant__ CUtensorMap map_ws, const RouterArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages;
   const int stage_bytes = kATileBytes + a.NE * kTileK * 2;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * stage_bytes);
+  const uint32_t C = gridDim.x;  // cluster size: the cluster spans blockIdx.x
+  const int region = max(S * stage_bytes, logit_buffer_bytes(a.NE, static_cast<int>(C)));
+  float* P = reinterpret_cast<float*>(smem);  // summed / partial logits, after the last MMA
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + region);
   uint64_t* empty = full + kMaxStages;
   uint64_t* acc_full = empty + kMaxStages;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * kTileM;
-  const int ks = blockIdx.y;
+  const uint32_t rank = C > 1 ? cluster_ctarank() : 0;
+  const int m0 = blockIdx.y * kTileM;
   const int KB = a.H / kTileK;
-  const int kb0 = ks * a.kb_per_split;
-  const int kb1 = min(KB, kb0 + a.kb_per_split);
+  const int kb0 = static_cast<int>(rank) * a.kb_per_cta;
+  const int kb1 = min(KB, kb0 + a.kb_per_cta);
   const int nboxes = a.n_wr_boxes + (a.gate_box >= 0 ? 1 : 0);
 
   pdl_trigger();
-  // x and the partial-logit scratch belong to earlier work of the stream;
-  // waiting before the TMEM allocation also means a kernel never holds TMEM
-  // while an earlier one on the same SM may still need some.
+  // x belongs to earlier work of the stream; waiting before the TMEM
+  // allocation also means a kernel never holds TMEM while an earlier one on
+  // the same SM may still need some.
   pdl_wait();
   if (threadIdx.x == 64) {
     for (int s = 0; s < S; ++s) {
@@ -118,217 +321,100 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma_commit(acc_full);
     }
-  } else {
-    // Epilogue: thread = token row (TMEM lane); write its NE partial logits.
-    if (mbar_wait(acc_full, 0, a.err, kSiteRouterEpilogue)) {
-      tc_fence_after_sync();
-      const int q = warp & 3;
-      const int row = m0 + q * 32 + lane;
-      float* dst = a.partial + (static_cast<size_t>(ks) * a.T + row) * a.NE;
-      for (int c0 = 0; c0 < a.NE; c0 += 32) {
-        uint32_t r[32];
-        const uint32_t ta = tmem_addr(tmem_base, q * 32, c0);
-        if (a.NE - c0 >= 32)
-          tmem_ld32(ta, r);
-        else
-          tmem_ld16(ta, r);
-        tmem_wait(r);
-        const int nc = min(32, a.NE - c0);
-        if (row < a.T) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            if (i < nc)
-              *reinterpret_cast<float4*>(dst + c0 + i) = make_float4(
-                  __uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-        }
-      }
-    }
-    tc_fence_before_sync();
+    __syncwarp();
   }
+  // Every CTA of the cluster reaches every cluster barrier, whatever happened
+  // above (a wait that gave up has recorded the error and the role stopped).
+  // Barrier 1: every MMA of the cluster has completed (the epilogue warps
+  // waited for their own accumulator), so every CTA's pipeline stages are free
+  // to receive partial logits.
+  bool acc_ok = true;
+  if (warp >= 2) {
+    acc_ok = mbar_wait(acc_full, 0, a.err, kSiteRouterEpilogue);
+    acc_ok = __all_sync(0xFFFFFFFFu, acc_ok);  // the TMEM loads below are warp-collective
+    tc_fence_after_sync();
+  }
+  __syncthreads();
+  if (C > 1) cluster_sync();
 
+  // Thread = token row (TMEM lane): its NE partial logits go to the CTA that
+  // owns the row, into slot `rank` of that CTA's buffer R[C][NE][ld].
+  const int rpc = kTileM / static_cast<int>(C);
+  const int ld = logit_ld(static_cast<int>(C));
+  const int slot_floats = a.NE * ld;
+  if (warp >= 2 && acc_ok) {
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t owner = static_cast<uint32_t>(row / rpc);
+    const int rr = row - static_cast<int>(owner) * rpc;  // row within the owner's share
+    float* slot = P + static_cast<size_t>(rank) * slot_floats;
+    const uint32_t dst = smem_u32(slot + rr);
+    const bool local = owner == rank || C == 1;
+    const uint32_t dst_c = local ? dst : mapa_shared(dst, owner);
+    for (int c0 = 0; c0 < a.NE; c0 += 32) {
+      uint32_t r[32];
+      const uint32_t ta = tmem_addr(tmem_base, q * 32, c0);
+      if (a.NE - c0 >= 32)
+        tmem_ld32(ta, r);
+      else
+        tmem_ld16(ta, r);
+      tmem_wait(r);
+      const int nc = min(32, a.NE - c0);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < nc) {
+          if (local)
+            slot[(c0 + i) * ld + rr] = __uint_as_float(r[i]);
+          else
+            asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst_c + 4u * (c0 + i) * ld), "r"(r[i])
+                         : "memory");
+        }
+    }
+  }
+  tc_fence_before_sync();
+  // Barrier 2: every partial row has arrived.  After it no CTA touches
+  // another's shared memory.
+  __syncthreads();
+  if (C > 1) cluster_sync();
+
+  // Owned rows: add the C partials in rank order into slot 0.
+  if (C > 1) {
+    const int n = rpc * a.NE;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const int c = i / rpc, r = i - c * rpc;
+      const int o = c * ld + r;
+      float v = P[o];
+      for (int src = 1; src < static_cast<int>(C); ++src) v += P[src * slot_floats + o];
+      P[o] = v;
+    }
+    __syncthreads();
+  }
+  // The logit bias, staged once per CTA after the partial-logit slots (when given).
+  float* bias_s = nullptr;
+  if (a.spec.logit_bias != nullptr) {
+    bias_s = P + static_cast<int>(C) * slot_floats;
+    for (int e = threadIdx.x; e < a.E; e += kThreads) bias_s[e] = a.spec.logit_bias[e];
+    __syncthreads();
+  }
+  // Selection: team i of 8 lanes takes owned rows i, i + 24, ...
+  constexpr int kTeams = kThreads / kTeam;
+  const int team = threadIdx.x / kTeam, tl = threadIdx.x % kTeam;
+  for (int base = 0; base < rpc; base += kTeams) {
+    if (base + (threadIdx.x & ~31) / kTeam >= rpc) break;  // whole warp past the owned rows
+    const int r = base + team, t = m0 + static_cast<int>(rank) * rpc + r;
+    const bool active = r < rpc && t < a.T;
+    const float* L = P + (r < rpc ? r : 0);
+    // two instantiations only: the kernel's code stays small (a few warps
+    // run this part; instruction fetch, not arithmetic, would bound it)
+    if (a.k <= 4)
+      select_team<4>(L, ld, bias_s, a, t, tl, active);
+    else
+      select_team<16>(L, ld, bias_s, a, t, tl, active);
+  }
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, a.tmem_cols);
-  }
-}
-
-// Warp-wide arg-max: the larger value wins, equal values go to the lower index.
-__device__ __forceinline__ void warp_best(float& v, int& i) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float v2 = __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    const int i2 = __shfl_xor_sync(0xFFFFFFFFu, i, o);
-    if (v2 > v || (v2 == v && i2 < i)) {
-      v = v2;
-      i = i2;
-    }
-  }
-}
-
-struct TopkArgs {
-  const float* partial;
-  int ksplit, T, NE, E, k, gate_col;
-  RouteSpec spec;
-  int32_t* topk_idx;
-  float* topk_w;
-  float* shared_scale;
-};
-
-__global__ void router_topk_kernel(const TopkArgs a) {
-  pdl_trigger();
-  pdl_wait();
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (t >= a.T) return;  // warp-uniform
-  const int E = a.E;
-  const bool sigmoid = a.spec.sigmoid != 0;
-
-  // Logit column c = lane + 32 j lives in l[j]; partials added in slice order.
-  float l[kJMax];
-#pragma unroll
-  for (int j = 0; j < kJMax; ++j) {
-    const int c = lane + 32 * j;
-    float v = -INFINITY;
-    if (c < a.NE) {
-      v = 0.f;
-      for (int s = 0; s < a.ksplit; ++s) v += a.partial[(static_cast<size_t>(s) * a.T + t) * a.NE + c];
-      if (c == a.gate_col) a.shared_scale[t] = 1.f / (1.f + __expf(-v));
-      if (c < E) {
-        if (a.spec.logit_bias != nullptr) v += a.spec.logit_bias[c];
-      } else {
-        v = -INFINITY;
-      }
-    }
-    l[j] = v;
-  }
-
-  // Softmax normaliser over all E logits (fixed butterfly order).
-  float mx = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < kJMax; ++j) mx = fmaxf(mx, l[j]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-  float se = 0.f;
-#pragma unroll
-  for (int j = 0; j < kJMax; ++j)
-    if (lane + 32 * j < E) se += __expf(l[j] - mx);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) se += __shfl_xor_sync(0xFFFFFFFFu, se, o);
-  const float inv_se = 1.f / se;
-  auto score = [&](float v) { return sigmoid ? 1.f / (1.f + __expf(-v)) : __expf(v - mx) * inv_se; };
-
-  // Group limiting: group score = sum of its top group_topn scores; keep the
-  // topk_group best groups (lane g holds group g's score).  Scores and group
-  // ids are computed once per column.
-  const int gsize = a.spec.n_group > 1 ? E / a.spec.n_group : E;
-  uint32_t kept = 0xFFFFFFFFu;
-  int gid[kJMax];
-  if (a.spec.n_group > 1) {
-    float sc[kJMax];
-#pragma unroll
-    for (int j = 0; j < kJMax; ++j) {
-      const int c = lane + 32 * j;
-      sc[j] = c < E ? score(l[j]) : -INFINITY;
-      gid[j] = c < E ? c / gsize : -1;  // no group
-    }
-    float my_gscore = -INFINITY;
-    if (gsize % 32 == 0 && a.spec.group_topn <= 2) {
-      // Group g is the columns j in [g*gpj, (g+1)*gpj) of every lane: each
-      // lane takes its own best two, then a butterfly merges the pairs
-      // (disjoint lane sets at every step, so nothing is counted twice).
-      const int gpj = gsize / 32;
-      for (int g = 0; g < a.spec.n_group; ++g) {
-        float b1 = -INFINITY, b2 = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < kJMax; ++j) {
-          if (j >= g * gpj && j < (g + 1) * gpj) {
-            const float v = sc[j];
-            if (v > b1) {
-              b2 = b1;
-              b1 = v;
-            } else if (v > b2) {
-              b2 = v;
-            }
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float p1 = __shfl_xor_sync(0xFFFFFFFFu, b1, o), p2 = __shfl_xor_sync(0xFFFFFFFFu, b2, o);
-          if (b1 >= p1) {
-            b2 = fmaxf(b2, p1);
-          } else {
-            b2 = fmaxf(p2, b1);
-            b1 = p1;
-          }
-        }
-        const float sum = a.spec.group_topn == 2 ? b1 + b2 : b1;
-        if (lane == g) my_gscore = sum;
-      }
-    } else {
-      for (int g = 0; g < a.spec.n_group; ++g) {
-        uint32_t taken = 0;
-        float sum = 0.f;
-        for (int r = 0; r < a.spec.group_topn; ++r) {
-          float v = -INFINITY;
-          int i = INT_MAX;
-#pragma unroll
-          for (int j = 0; j < kJMax; ++j) {
-            const int c = lane + 32 * j;
-            if (gid[j] == g && !((taken >> j) & 1u) && (sc[j] > v || (sc[j] == v && c < i))) {
-              v = sc[j];
-              i = c;
-            }
-          }
-          warp_best(v, i);
-          sum += v;
-          if (i != INT_MAX && (i & 31) == lane) taken |= 1u << (i >> 5);
-        }
-        if (lane == g) my_gscore = sum;
-      }
-    }
-    kept = 0;
-    for (int r = 0; r < a.spec.topk_group; ++r) {
-      float v = (lane < a.spec.n_group && !((kept >> lane) & 1u)) ? my_gscore : -INFINITY;
-      int i = lane < a.spec.n_group ? lane : INT_MAX;
-      warp_best(v, i);
-      if (i != INT_MAX) kept |= 1u << i;
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < kJMax; ++j) gid[j] = 0;
-  }
-
-  // k rounds of warp arg-max over the candidate logits (the score functions
-  // are monotone, so ordering by logit is ordering by score).
-  uint32_t taken = 0;
-  int my_idx = 0;
-  float my_score = 0.f, sum = 0.f;
-  for (int r = 0; r < a.k; ++r) {
-    float v = -INFINITY;
-    int i = INT_MAX;
-#pragma unroll
-    for (int j = 0; j < kJMax; ++j) {
-      const int c = lane + 32 * j;
-      if (c < E && ((kept >> gid[j]) & 1u) && !((taken >> j) & 1u)) {
-        if (l[j] > v || (l[j] == v && c < i)) {
-          v = l[j];
-          i = c;
-        }
-      }
-    }
-    warp_best(v, i);
-    if (i != INT_MAX && (i & 31) == lane) taken |= 1u << (i >> 5);
-    const float sc = score(v);
-    sum += sc;
-    if (lane == r) {
-      my_idx = i;
-      my_score = sc;
-    }
-  }
-  if (lane < a.k) {
-    const float scale = a.spec.renormalize ? a.spec.route_scale / sum : a.spec.route_scale;
-    a.topk_idx[static_cast<size_t>(t) * a.k + lane] = my_idx;
-    a.topk_w[static_cast<size_t>(t) * a.k + lane] = my_score * scale;
   }
 }
 
@@ -366,74 +452,76 @@ RouterPlan router_plan(int T, int H, int E, bool shared_gate) {
   const int ne_wr = (E + 15) / 16 * 16;
   p.fused_gate = shared_gate && ne_wr + 16 <= 256;
   p.NE = ne_wr + (p.fused_gate ? 16 : 0);
-  const int m_tiles = (T + kTileM - 1) / kTileM;
+  p.m_tiles = (T + kTileM - 1) / kTileM;
   const int KB = H / kTileK;
-  // Enough K slices to put ~152 CTAs to work, at least 2 k-blocks each, and at
-  // most ~32 MB of partial logits.  Depends on the shapes only.
-  int ks = 152 / (m_tiles > 0 ? m_tiles : 1);
-  if (ks > KB / 2) ks = KB / 2;
-  const long long per_slice = static_cast<long long>(T) * p.NE * 4;
-  if (per_slice > 0 && ks * per_slice > (32ll << 20)) ks = static_cast<int>((32ll << 20) / per_slice);
-  if (ks < 1) ks = 1;
-  const int kbs = (KB + ks - 1) / ks;
-  p.ksplit = (KB + kbs - 1) / kbs;
-  p.kb_per_split = kbs;
-  p.scratch_bytes = static_cast<size_t>(p.ksplit) * per_slice;
+  // The largest power-of-two cluster (<= 8) that keeps the grid within one
+  // wave of ~152 CTAs and leaves every CTA at least two K blocks, so that the
+  // W_r stream of a small batch spreads over several SMs.  Shapes only.
+  int c = 1;
+  while (c < kMaxCluster && p.m_tiles * (2 * c) <= 152 && KB / (2 * c) >= 2) c <<= 1;
+  p.kb_per_cta = (KB + c - 1) / c;
+  while (c > 1 && (c - 1) * p.kb_per_cta >= KB) c >>= 1;  // every CTA gets a K block
+  p.kb_per_cta = (KB + c - 1) / c;
+  p.cluster = c;
   return p;
+}
+
+int router_launches(int T, int H, int E, bool shared_gate) {
+  if (T == 0) return 0;
+  const RouterPlan p = router_plan(T, H, E, shared_gate);
+  return 1 + ((shared_gate && !p.fused_gate) ? 1 : 0);
 }
 
 cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_wr, const CUtensorMap* map_ws, int T,
                           int H, int E, int k, const RouteSpec& spec, const void* x, const void* w_shared_gate,
-                          int32_t* topk_idx, float* topk_w, float* shared_scale, void* scratch, uint32_t* err,
+                          int32_t* topk_idx, float* topk_w, float* shared_scale, uint32_t* err,
                           cudaStream_t stream) {
-  const RouterPlan p = router_plan(T, H, E, w_shared_gate != nullptr && shared_scale != nullptr);
-  GemmArgs g{};
+  if (T == 0) return cudaSuccess;
+  const bool gate = w_shared_gate != nullptr && shared_scale != nullptr;
+  const RouterPlan p = router_plan(T, H, E, gate);
+  RouterArgs g{};
   g.T = T;
   g.H = H;
+  g.E = E;
+  g.k = k;
   g.NE = p.NE;
   g.n_wr_boxes = (E + 15) / 16;
   g.gate_box = p.fused_gate ? g.n_wr_boxes : -1;
+  g.gate_col = p.fused_gate ? g.n_wr_boxes * 16 : -1;
   g.tmem_cols = p.NE <= 32 ? 32 : p.NE <= 64 ? 64 : p.NE <= 128 ? 128 : 256;
-  g.kb_per_split = p.kb_per_split;
-  g.partial = static_cast<float*>(scratch);
+  g.kb_per_cta = p.kb_per_cta;
+  g.spec = spec;
+  g.topk_idx = topk_idx;
+  g.topk_w = topk_w;
+  g.shared_scale = shared_scale;
   g.err = err;
   const int stage_bytes = kATileBytes + p.NE * kTileK * 2;
   const int fixed = 1024 + (2 * kMaxStages + 2) * 8 + 64;
   int stages = (227 * 1024 - fixed) / stage_bytes;
   if (stages > kMaxStages) stages = kMaxStages;
-  if (stages > p.kb_per_split) stages = p.kb_per_split;
+  if (stages > p.kb_per_cta) stages = p.kb_per_cta;
   g.stages = stages;
-  const size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(stages) * stage_bytes;
+  const int lbuf = logit_buffer_bytes(p.NE, p.cluster);
+  const int region = stages * stage_bytes > lbuf ? stages * stage_bytes : lbuf;
+  // At least half an SM's shared memory, so that one router CTA at most runs
+  // on an SM: a CTA that waits at a cluster barrier then never holds TMEM
+  // another cluster's CTA on the same SM is waiting to allocate.
+  size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(region);
+  if (smem < 116 * 1024) smem = 116 * 1024;
 
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const dim3 grid((T + kTileM - 1) / kTileM, p.ksplit);
-  cudaError_t e = launch_kernel(router_gemm_kernel, grid, dim3(kThreads), smem, stream, map_x, map_wr,
-                                p.fused_gate ? *map_ws : map_wr, g);
+  const dim3 grid(p.cluster, p.m_tiles);
+  cudaError_t e = launch_kernel_cluster(router_kernel, grid, dim3(kThreads), smem, stream, p.cluster, map_x, map_wr,
+                                        p.fused_gate ? *map_ws : map_wr, g);
   if (e != cudaSuccess) return e;
-
-  TopkArgs t{};
-  t.partial = g.partial;
-  t.ksplit = p.ksplit;
-  t.T = T;
-  t.NE = p.NE;
-  t.E = E;
-  t.k = k;
-  t.gate_col = p.fused_gate ? g.n_wr_boxes * 16 : -1;
-  t.spec = spec;
-  t.topk_idx = topk_idx;
-  t.topk_w = topk_w;
-  t.shared_scale = shared_scale;
-  const int warps = 8;
-  e = launch_kernel(router_topk_kernel, dim3((T + warps - 1) / warps), dim3(warps * 32), 0, stream, t);
-  if (e != cudaSuccess) return e;
-  if (w_shared_gate != nullptr && shared_scale != nullptr && !p.fused_gate) {
+  if (gate && !p.fused_gate) {
     e = launch_kernel(shared_gate_kernel, dim3((T * 32 + 255) / 256), dim3(256), 0, stream,
                       static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_shared_gate), T, H,
                       shared_scale);

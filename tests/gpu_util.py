@@ -22,6 +22,10 @@ def dev_f32(a) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to("cuda")
 
 
+def dev_f16(a) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float16)).to("cuda")
+
+
 def dev_i32(a) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to("cuda")
 
@@ -92,13 +96,27 @@ def check_routing(wl, gpu_idx: np.ndarray, gpu_w: np.ndarray, orc: dict) -> np.n
     return same
 
 
-def compare_outputs(gpu_out: np.ndarray, orc_out: np.ndarray, what: str = "out"):
-    """rel-L2 and max-abs over all compared elements (both in float64)."""
+def compare_outputs(gpu_out: np.ndarray, orc_out: np.ndarray, what: str = "out", scaled: bool = False):
+    """rel-L2 and max-abs over all compared elements (both in float64).
+
+    The five layer shapes use the fixed bounds (rel-L2 1e-2, max-abs 5e-2).
+    ``scaled`` (the other shapes, whose outputs reach |out| >= 16, where the
+    bf16 output's own rounding alone can cost 2^-8 |out| > 5e-2): element by
+    element |gpu - oracle| <= max(5e-2, 2^-8 |oracle| + 2e-2), i.e. half a bf16
+    ulp of the value plus the computation's own error budget.
+    """
     diff = gpu_out - orc_out
     rel = np.linalg.norm(diff) / max(np.linalg.norm(orc_out), 1e-300)
     mx = float(np.abs(diff).max()) if diff.size else 0.0
     assert rel <= REL_L2_TOL, f"{what}: rel-L2 {rel:.3e} > {REL_L2_TOL}"
-    assert mx <= MAX_ABS_TOL, f"{what}: max-abs {mx:.3e} > {MAX_ABS_TOL}"
+    if scaled:
+        bound = np.maximum(MAX_ABS_TOL, 2.0 ** -8 * np.abs(orc_out) + 2e-2)
+        worst = np.unravel_index(np.argmax(np.abs(diff) - bound), diff.shape) if diff.size else None
+        assert np.all(np.abs(diff) <= bound), \
+            f"{what}: |diff| {abs(diff[worst]):.3e} > {bound[worst]:.3e} at |oracle| {abs(orc_out[worst]):.3f}"
+    else:
+        assert mx <= MAX_ABS_TOL, f"{what}: max-abs {mx:.3e} > {MAX_ABS_TOL} (max |oracle| " \
+                                  f"{float(np.abs(orc_out).max()):.2f})"
     return rel, mx
 
 
@@ -141,7 +159,8 @@ def tile_targeted_tokens(counts, perm, k, T, n_random=16, boxes=(512, 256, 128, 
     return np.unique(np.concatenate([toks, rnd, [0, T - 1]]).astype(np.int64))
 
 
-def check_forward(wl, inp: dict, d: dict, out: torch.Tensor, cfg, tokens=None, orc_route=None) -> dict:
+def check_forward(wl, inp: dict, d: dict, out: torch.Tensor, cfg, tokens=None, orc_route=None,
+                  scaled=False) -> dict:
     """Parity of one layer forward with the oracle.
 
     1. Routing of every token (check_routing).
@@ -182,8 +201,8 @@ def check_forward(wl, inp: dict, d: dict, out: torch.Tensor, cfg, tokens=None, o
         ref = oracle.forward_tokens(inp, wl, tokens, forced_idx=forced[tokens])["out"]
         got_out = host_f64(out)[tokens]
     assert np.all(np.isfinite(got_out))
-    rel, mx = compare_outputs(got_out, ref)
-    return {"rel_l2": rel, "max_abs": mx, "flipped": int((~same).sum()), "identical_routing": identical,
+    rel, mx = compare_outputs(got_out, ref, scaled=scaled)
+    return {"rel_l2": rel, "max_abs": mx, "max_abs_out": float(np.abs(ref).max()), "flipped": int((~same).sum()), "identical_routing": identical,
             "rows_compared": int(got_out.shape[0]), "counts": c, "perm": p}
 
 

@@ -89,18 +89,22 @@ def test_forward_config_point(name, T, alpha, mode):
         cap = 6 if wl.E > 64 else None
         tokens = lambda c, p: tile_targeted_tokens(c, p, wl.k, T, n_random=16, cap_per_expert=cap)  # noqa: E731
     r = check_forward(wl, inp, d, out, cfg, tokens=tokens)
-    print(f"{wl.label}: {r['rows_compared']} rows, rel-L2 {r['rel_l2']:.2e} max-abs {r['max_abs']:.2e}, "
-          f"near-tie flips {r['flipped']}, routing identical to the oracle's: {r['identical_routing']}")
+    print(f"{wl.label}: {r['rows_compared']} rows, rel-L2 {r['rel_l2']:.2e} max-abs {r['max_abs']:.2e} "
+          f"(max |out| {r['max_abs_out']:.1f}), near-tie flips {r['flipped']}, routing identical to the "
+          f"oracle's: {r['identical_routing']}")
 
 
-# The Mixtral-8x22B shape (second Mixtral layer of the review's tables).
+# The Mixtral-8x22B shape (second Mixtral layer of the review's tables).  Its
+# outputs reach |out| >= 16, where the bf16 output's rounding alone exceeds
+# 5e-2: the element-wise bound scales with the value (compare_outputs).
 @pytest.mark.parametrize("T", [32, 4096])
 def test_forward_mixtral22b(T):
     wl, inp, d = _inputs("mixtral22b", T, None)
     out, cfg = _run(wl, d)
     tokens = None if T <= 32 else (lambda c, p: tile_targeted_tokens(c, p, wl.k, T, n_random=16))
-    r = check_forward(wl, inp, d, out, cfg, tokens=tokens)
-    print(f"{wl.label}: {r['rows_compared']} rows, rel-L2 {r['rel_l2']:.2e} max-abs {r['max_abs']:.2e}")
+    r = check_forward(wl, inp, d, out, cfg, tokens=tokens, scaled=True)
+    print(f"{wl.label}: {r['rows_compared']} rows, rel-L2 {r['rel_l2']:.2e} max-abs {r['max_abs']:.2e} "
+          f"(max |out| {r['max_abs_out']:.1f})")
 
 
 @pytest.mark.parametrize("name,T,kw", [("tiny", 128, {}), ("qwen2", 96, {}), ("deepseek", 256, {"E": 32})],

@@ -12,7 +12,8 @@ import oracle
 import synth
 from synth.workloads import Workload
 
-from gpu_util import (check_routing, dev_bf16, dev_f32, dev_i32, device_inputs, host_bits, host_f64, make_cfg)
+from gpu_util import (check_routing, dev_bf16, dev_f16, dev_f32, dev_i32, device_inputs, host_bits, host_f64,
+                      make_cfg)
 
 pytestmark = pytest.mark.gpu
 
@@ -288,28 +289,31 @@ def test_dense_ffn_matches_plain_swiglu():
 # ----------------------------------------------------------------------------- combine
 
 @pytest.mark.parametrize("T,k,H,shared", [(1, 2, 128, False), (129, 2, 512, False), (300, 8, 384, True),
-                                          (64, 4, 2048, True)])
+                                          (64, 4, 2048, True), (4100, 8, 256, True)])
 def test_combine(T, k, H, shared):
+    """Inputs are fp16 expert outputs (as moe_expert_ffn writes them)."""
     E = 16
     idx = synth.random_topk(5, T, E, k)
     _, _, perm, inv = oracle.permute(idx, E)
-    y_perm = synth.normal_f64(5, 70, (T * k, H)).astype(np.float32)
+    y_perm = synth.normal_f64(5, 70, (T * k, H)).astype(np.float16)
     w = synth.uniform01(5, 71, T * k).reshape(T, k).astype(np.float32)
-    ys = synth.normal_f64(5, 72, (T, H)).astype(np.float32) if shared else None
+    ys = synth.normal_f64(5, 72, (T, H)).astype(np.float16) if shared else None
     sc = synth.uniform01(5, 73, T).astype(np.float32) if shared else None
-    out = moe.moe_combine(dev_f32(y_perm), dev_i32(inv), dev_f32(w), dev_f32(ys) if shared else None,
-                          dev_f32(sc) if shared else None)
+
+    def run():
+        return moe.moe_combine(dev_f16(y_perm), dev_i32(inv), dev_f32(w), dev_f16(ys) if shared else None,
+                               dev_f32(sc) if shared else None)
+
+    out = run()
     Y = y_perm.astype(np.float64)[inv.reshape(T, k)]
     want = oracle.combine(Y, w.astype(np.float64))
     if shared:
-        want = want + sc.astype(np.float64)[:, None] * ys
+        want = want + sc.astype(np.float64)[:, None] * ys.astype(np.float64)
     got = host_f64(out)
     # fp32 sum of k+1 terms rounded once to bf16
     assert np.all(np.abs(got - want) <= 2.0 ** -8 * np.abs(want) + 1e-5)
     # deterministic: a second call gives identical bits
-    out2 = moe.moe_combine(dev_f32(y_perm), dev_i32(inv), dev_f32(w), dev_f32(ys) if shared else None,
-                           dev_f32(sc) if shared else None)
-    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(out.view(torch.int16), run().view(torch.int16))
 
 
 # ----------------------------------------------------------------------------- failure path
