@@ -321,8 +321,11 @@ MOE_API moe_status_t moe_selftest_wait_timeout(uint32_t limit_us, moe_stream_t s
  * any stream records events[i] (cudaEvent_t handles created by the caller)
  * on its stream just before stage i and events[count-1] after the last:
  * stage 0 route (router GEMM + top-k, shared gate), 1 permute, 2 gate+up
- * GEMM, 3 down GEMM, 4 combine; count must be 6.  Pass NULL/0 to switch it
- * off.  Process-wide setting meant for profiling; not thread-safe.
+ * GEMM, 3 down GEMM, 4 combine; count must be 6.  An entry may be NULL (no
+ * event at that boundary; not all of them).  Pass NULL/0 to switch it off.
+ * An event between two kernels ends the launch overlap between them, so
+ * record only the boundaries you need.  Process-wide setting meant for
+ * profiling; not thread-safe.
  */
 MOE_API moe_status_t moe_set_trace_events(void* const* events, int count);
 

@@ -358,15 +358,16 @@ def moe_launches_issued() -> int:
 
 
 def moe_set_trace_events(events):
-    """Record the given 6 torch.cuda.Event objects around the stages of later forwards; None turns it off."""
+    """Record the given 6 torch.cuda.Event objects (None entries: no event at that
+    boundary) around the stages of later forwards; None turns it off."""
     lib = load_library()
     if events is None:
         _check(lib.moe_set_trace_events(None, 0), "moe_set_trace_events")
         return
     for e in events:
-        if not e.cuda_event:  # torch creates the CUDA event on first record
+        if e is not None and not e.cuda_event:  # torch creates the CUDA event on first record
             e.record()
-    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event if e is not None else None for e in events])
     _check(lib.moe_set_trace_events(arr, len(events)), "moe_set_trace_events")
 
 

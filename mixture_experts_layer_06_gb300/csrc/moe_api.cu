@@ -58,7 +58,7 @@ cudaEvent_t g_trace[kTraceEvents] = {};
 bool g_trace_on = false;
 
 void trace(int i, cudaStream_t s) {
-  if (g_trace_on) cudaEventRecord(g_trace[i], s);
+  if (g_trace_on && g_trace[i] != nullptr) cudaEventRecord(g_trace[i], s);
 }
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -571,10 +571,10 @@ moe_status_t moe_set_trace_events(void* const* events, int count) {
     return MOE_OK;
   }
   if (count != kTraceEvents) return MOE_ERR_INVALID_VALUE;
-  for (int i = 0; i < kTraceEvents; ++i) {
-    if (events[i] == nullptr) return MOE_ERR_INVALID_VALUE;
-    g_trace[i] = static_cast<cudaEvent_t>(events[i]);
-  }
+  bool any = false;
+  for (int i = 0; i < kTraceEvents; ++i) any = any || events[i] != nullptr;
+  if (!any) return MOE_ERR_INVALID_VALUE;
+  for (int i = 0; i < kTraceEvents; ++i) g_trace[i] = static_cast<cudaEvent_t>(events[i]);
   g_trace_on = true;
   return MOE_OK;
 }

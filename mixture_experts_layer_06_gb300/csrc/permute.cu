@@ -244,13 +244,22 @@ __global__ void __launch_bounds__(kSmallThreads)
       if (r >= 0) perm[r] = q;
       inv[q] = r;
     }
-  // x_perm: CTA b copies the rows of copies b, b + gridDim.x, ... (16-byte pieces)
+  // x_perm: CTA b copies the rows of copies b, b + gridDim.x, ... in 16-byte
+  // pieces, four loads in flight per thread
   for (int q = blockIdx.x; q < rows; q += gridDim.x) {
     const int r = row_of(q);  // the same for every thread of the CTA
     if (r < 0) continue;
     const uint4* src = x + static_cast<size_t>(q / k) * H8;
     uint4* dst = x_perm + static_cast<size_t>(r) * H8;
-    for (int v = tid; v < H8; v += kSmallThreads) dst[v] = src[v];
+    for (int v0 = tid; v0 < H8; v0 += 4 * kSmallThreads) {
+      uint4 val[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v0 + u * kSmallThreads < H8) val[u] = src[v0 + u * kSmallThreads];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v0 + u * kSmallThreads < H8) dst[v0 + u * kSmallThreads] = val[u];
+    }
   }
 }
 
@@ -269,8 +278,8 @@ cudaError_t launch_permute(const int32_t* topk_idx, const void* x, int T, int H,
                            int32_t* offsets, int32_t* perm, int32_t* inv, void* x_perm, void* scratch,
                            uint32_t* err, cudaStream_t stream) {
   if (permute_is_small(T, E)) {
-    long long g = static_cast<long long>(T) * k;  // one CTA per copied row, at most one wave
-    if (g > 148) g = 148;
+    long long g = static_cast<long long>(T) * k;  // one CTA per copied row, up to 4 per SM
+    if (g > 4 * 148) g = 4 * 148;
     if (g < 1) g = 1;
     return launch_kernel(permute_small_kernel, dim3(static_cast<unsigned>(g)), dim3(kSmallThreads), 0, stream,
                          topk_idx, static_cast<const uint4*>(x), T, H / 8, E, k, counts, offsets, perm, inv,

@@ -78,12 +78,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait for the phase of `bar` with the given parity to complete, for at most
 // limit_ns.  Returns false (and records the site) if it gave up.
+#ifndef MOE_WAIT_CLOCK_EVERY
+#define MOE_WAIT_CLOCK_EVERY 1  // polls between reads of the timer (a power of two)
+#endif
 __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns, uint32_t* err,
                                               uint32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  uint32_t n = 0;
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > limit_ns) {
+    if ((++n & (MOE_WAIT_CLOCK_EVERY - 1)) == 0 && globaltimer_ns() - t0 > limit_ns) {
       raise_error(err, kErrTimeout, site);
       return false;
     }

@@ -53,6 +53,7 @@ __host__ __device__ constexpr int logit_ld(int C) { return kTileM / C + 4; }
 __host__ __device__ constexpr int logit_buffer_bytes(int NE, int C) { return C * NE * logit_ld(C) * 4 + 256 * 4; }
 
 constexpr int kTeam = 8;  // lanes that select the experts of one token
+constexpr int kMaxPerLane = 256 / kTeam;  // experts per lane (E <= 256)
 
 __device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
   return v1 > v2 || (v1 == v2 && i1 < i2);
@@ -64,8 +65,7 @@ __device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
 // score functions are monotone, so experts (and a group's top scores) are
 // ranked by logit; scores are evaluated only where a value is needed.  Ties
 // go to the lower expert (group) index.  Every lane of the warp calls this
-// (the shuffles span the warp); only `active` teams write.  KMAX >= k.
-template <int KMAX>
+// (the shuffles span the warp); only `active` teams write.
 __device__ void select_team(const float* L, int ld, const float* bias, const RouterArgs& a, int t, int tl,
                             bool active) {
   const int E = a.E, k = a.k;
@@ -152,50 +152,44 @@ __device__ void select_team(const float* L, int ld, const float* bias, const Rou
     }
   }
 
-  // This lane's best KMAX candidates by logit, descending (lower id first
-  // among equals: the experts are scanned in increasing order).
-  float bv[KMAX];
-  int bi[KMAX];
+  // This lane's candidates (experts tl + 8j of the kept groups) in registers.
+  float lv[kMaxPerLane];
+  {
+    int g = 0, gend = gsize;
 #pragma unroll
-  for (int j = 0; j < KMAX; ++j) {
-    bv[j] = -INFINITY;
-    bi[j] = INT_MAX;
-  }
-  int g = 0, gend = gsize;
-  for (int e = tl; e < E; e += kTeam) {
-    while (e >= gend) {
-      ++g;
-      gend += gsize;
-    }
-    if (!((kept >> g) & 1u)) continue;
-    const float v = logit(e);
-    if (v > bv[KMAX - 1] || bi[KMAX - 1] == INT_MAX) {
-      bv[KMAX - 1] = v;
-      bi[KMAX - 1] = e;
-#pragma unroll
-      for (int j = KMAX - 1; j > 0; --j) {
-        if (bv[j] > bv[j - 1] || (bi[j - 1] == INT_MAX && bi[j] != INT_MAX)) {
-          const float tv = bv[j];
-          bv[j] = bv[j - 1];
-          bv[j - 1] = tv;
-          const int ti = bi[j];
-          bi[j] = bi[j - 1];
-          bi[j - 1] = ti;
+    for (int j = 0; j < kMaxPerLane; ++j) {
+      const int e = tl + kTeam * j;
+      lv[j] = -INFINITY;
+      if (e < E) {
+        while (e >= gend) {
+          ++g;
+          gend += gsize;
         }
+        if ((kept >> g) & 1u) lv[j] = logit(e);
       }
     }
   }
 
-  // k rounds: the team's best head wins the round; its lane pops it.  The
-  // weights are the scores of the k winners, renormalised over them when
-  // asked (a renormalised softmax needs only the winners' logits: its
-  // denominator cancels), times the routed scaling factor.
+  // k rounds: each lane offers its best candidate not taken yet (the lowest
+  // j among equals: the lower expert id), the team's best wins the round and
+  // its lane marks it taken.  The weights are the scores of the k winners,
+  // renormalised over them when asked (a renormalised softmax needs only the
+  // winners' logits: its denominator cancels), times the routed scaling factor.
   const bool renorm_softmax = !sigmoid && a.spec.renormalize && ng == 1;
+  uint32_t taken = 0;
   float v0 = 0.f, sum = 0.f, s_lo = 0.f, s_hi = 0.f;
   int i_lo = -1, i_hi = -1;
   for (int r = 0; r < k; ++r) {
-    float v = bv[0];
-    int i = bi[0];
+    float v = -INFINITY;
+    int jb = -1;
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j)
+      if (!((taken >> j) & 1u) && lv[j] != -INFINITY && (jb < 0 || lv[j] > v)) {
+        v = lv[j];
+        jb = j;
+      }
+    int i = jb >= 0 ? tl + kTeam * jb : INT_MAX;
+    const int mine = i;
 #pragma unroll
     for (int o = kTeam / 2; o > 0; o >>= 1) {
       const float v2 = __shfl_xor_sync(0xFFFFFFFFu, v, o);
@@ -205,15 +199,7 @@ __device__ void select_team(const float* L, int ld, const float* bias, const Rou
         i = i2;
       }
     }
-    if (i == bi[0] && i != INT_MAX) {  // this lane's head won: pop it
-#pragma unroll
-      for (int j = 0; j < KMAX - 1; ++j) {
-        bv[j] = bv[j + 1];
-        bi[j] = bi[j + 1];
-      }
-      bv[KMAX - 1] = -INFINITY;
-      bi[KMAX - 1] = INT_MAX;
-    }
+    if (jb >= 0 && i == mine) taken |= 1u << jb;
     if (r == 0) v0 = v;
     const float sc = renorm_softmax ? __expf(v - v0) : score(v);
     sum += sc;
@@ -379,13 +365,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Owned rows: add the C partials in rank order into slot 0.
   if (C > 1) {
-    const int n = rpc * a.NE;
+    // 4 consecutive rows of one column per thread (rpc and ld are multiples of 4)
+    const int q4 = rpc / 4, n = q4 * a.NE;
     for (int i = threadIdx.x; i < n; i += kThreads) {
-      const int c = i / rpc, r = i - c * rpc;
-      const int o = c * ld + r;
-      float v = P[o];
-      for (int src = 1; src < static_cast<int>(C); ++src) v += P[src * slot_floats + o];
-      P[o] = v;
+      const int c = i / q4, r = (i - c * q4) * 4;
+      float4* dst = reinterpret_cast<float4*>(P + c * ld + r);
+      float4 v = *dst;
+      for (int src = 1; src < static_cast<int>(C); ++src) {
+        const float4 w = *reinterpret_cast<const float4*>(P + src * slot_floats + c * ld + r);
+        v.x += w.x;
+        v.y += w.y;
+        v.z += w.z;
+        v.w += w.w;
+      }
+      *dst = v;
     }
     __syncthreads();
   }
@@ -404,12 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = base + team, t = m0 + static_cast<int>(rank) * rpc + r;
     const bool active = r < rpc && t < a.T;
     const float* L = P + (r < rpc ? r : 0);
-    // two instantiations only: the kernel's code stays small (a few warps
-    // run this part; instruction fetch, not arithmetic, would bound it)
-    if (a.k <= 4)
-      select_team<4>(L, ld, bias_s, a, t, tl, active);
-    else
-      select_team<16>(L, ld, bias_s, a, t, tl, active);
+    select_team(L, ld, bias_s, a, t, tl, active);
   }
   __syncthreads();
   if (warp == 1) {

@@ -119,7 +119,10 @@ def test_zero_tokens_is_a_noop(lib):
 def test_trace_event_argument_check(lib):
     assert lib.moe_set_trace_events(None, 0) == 0
     arr = (ctypes.c_void_p * 3)(1, 2, 3)
-    assert lib.moe_set_trace_events(arr, 3) == 1
+    assert lib.moe_set_trace_events(arr, 3) == 1  # six boundaries, not three
+    none = (ctypes.c_void_p * 6)()
+    assert lib.moe_set_trace_events(none, 6) == 1  # at least one event
+    assert lib.moe_set_trace_events(None, 0) == 0
 
 
 def test_package_has_no_cpu_fallback():
