@@ -299,6 +299,8 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
         for (int i = 0; i < maps.seg[sg].nb; ++i) tma_prefetch_map(&maps.seg[sg].b[i]);
       }
       bool ok = true;
+      int ps = 0;        // ring slot of stage `it` (it % S, kept as a running counter:
+      uint32_t pph = 0;  // a division per stage is not free on the issue path) and its phase
       for (int tile = first; tile < total && ok; tile += stride) {
         const Tile t = decode_tile(a, sc, tile);
         const SegMaps& ms = maps.seg[t.s];
@@ -311,8 +313,12 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
         const CUtensorMap* mb = &ms.b[bi];
         const uint32_t bytes = BDIV * KPS * (NSUB * kATileBytes + (bi + 1) * ms.bstep * kTileK * 2);
         for (int kb = t.kb0; kb < t.kb1; ++kb, ++it) {
-          const int s = it % S;
-          const uint32_t ph = (it / S) & 1;
+          const int s = ps;
+          const uint32_t ph = pph;
+          if (++ps == S) {
+            ps = 0;
+            pph ^= 1;
+          }
           if (!mbar_wait(&empty[s], ph ^ 1, a.err, kSiteGemmProducer)) {
             ok = false;
             break;
@@ -392,7 +398,9 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && rank == 0) {
-      int it = 0, n = 0;
+      int n = 0;
+      int ms_ = 0;       // ring slot and phase of the next stage (running counters)
+      uint32_t mph = 0;
       bool ok = true;
       for (int tile = first; tile < total && ok; tile += stride, ++n) {
         const Tile t = decode_tile(a, sc, tile);
@@ -406,9 +414,13 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
         // consecutive K blocks of the token box lie box-rows * 128 bytes apart
         const SegMaps& ms = maps.seg[t.s];
         const uint32_t b_atom = (box_index(ms, n_tile / BDIV) + 1) * ms.bstep * kTileK * 2;
-        for (int kb = t.kb0; kb < t.kb1; ++kb, ++it) {
-          const int s = it % S;
-          const uint32_t ph = (it / S) & 1;
+        for (int kb = t.kb0; kb < t.kb1; ++kb) {
+          const int s = ms_;
+          const uint32_t ph = mph;
+          if (++ms_ == S) {
+            ms_ = 0;
+            mph ^= 1;
+          }
           if (!mbar_wait(&full[s], ph, a.err, kSiteGemmMma)) {
             ok = false;
             break;

@@ -97,11 +97,20 @@ cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_wr, c
 // Launches of launch_router for these shapes.
 int router_launches(int T, int H, int E, bool shared_gate);
 
+// Decode-sized batches: routing and the permutation (counts, offsets, perm,
+// inv, x_perm) in one single-CTA launch on the CUDA cores, when
+// route_permute_is_tiny (T <= 8 and E * H <= 128K router weights).
+bool route_permute_is_tiny(int T, int H, int E, int k);
+cudaError_t launch_route_permute_tiny(int T, int H, int E, int k, const RouteSpec& spec, const void* x,
+                                      const void* w_router, const void* w_shared_gate, int32_t* topk_idx,
+                                      float* topk_w, float* shared_scale, int32_t* counts, int32_t* offsets,
+                                      int32_t* perm, int32_t* inv, void* x_perm, cudaStream_t stream);
+
 // Permutation: bitmap build, scan, gather (see permute.cu); one launch for
 // small batches (permute_is_small), which then uses no scratch.
 size_t permute_scratch_bytes(int T, int E);
-bool permute_is_small(int T, int E);
-int permute_launches(int T, int E);
+bool permute_is_small(int T, int E, int k);
+int permute_launches(int T, int E, int k);
 cudaError_t launch_permute(const int32_t* topk_idx, const void* x, int T, int H, int E, int k, int32_t* counts,
                            int32_t* offsets, int32_t* perm, int32_t* inv, void* x_perm, void* scratch,
                            uint32_t* err, cudaStream_t stream);

@@ -531,10 +531,11 @@ moe_status_t ffn_static_impl(DeviceState* d, const FfnOperands& o, int block_m, 
 }
 
 // Kernels moe_forward_ex launches for these shapes (its launch sequence below).
-int forward_launches(const moe_config_t& c, int T, int H, int E) {
+int forward_launches(const moe_config_t& c, int T, int H, int E, int k) {
   if (T == 0) return 0;
-  const int route = moe::router_launches(T, H, E, c.w_shared_gate != nullptr);
-  const int permute = moe::permute_launches(T, E);
+  const bool tiny = moe::route_permute_is_tiny(T, H, E, k);
+  const int route = tiny ? 1 : moe::router_launches(T, H, E, c.w_shared_gate != nullptr);
+  const int permute = tiny ? 0 : moe::permute_launches(T, E, k);
   const int ffn = 2;
   const int combine = 1;
   return route + permute + ffn + combine;
@@ -760,12 +761,20 @@ moe_status_t moe_forward_ex(const moe_config_t* cfg, const void* x, const void* 
   const int Tk = T * k;
 
   trace(0, s);
-  if ((st = route_impl(d, c, x, w_router, T, H, E, k, topk_idx, topk_w, shared_scale, s)) != MOE_OK)
-    return st;
-  trace(1, s);
-  if ((st = permute_impl(d, topk_idx, x, T, H, E, k, static_cast<int32_t*>(at(L.counts)), offsets,
-                         static_cast<int32_t*>(at(L.perm)), inv, at(L.x_perm), at(L.scratch), s)) != MOE_OK)
-    return st;
+  if (moe::route_permute_is_tiny(T, H, E, k)) {
+    // decode-sized batch: routing and grouping in one launch (the permute stage is empty)
+    if (moe::launch_route_permute_tiny(T, H, E, k, route_spec(c), x, w_router, c.w_shared_gate, topk_idx, topk_w,
+                                       shared_scale, static_cast<int32_t*>(at(L.counts)), offsets,
+                                       static_cast<int32_t*>(at(L.perm)), inv, at(L.x_perm), s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    trace(1, s);
+  } else {
+    if ((st = route_impl(d, c, x, w_router, T, H, E, k, topk_idx, topk_w, shared_scale, s)) != MOE_OK) return st;
+    trace(1, s);
+    if ((st = permute_impl(d, topk_idx, x, T, H, E, k, static_cast<int32_t*>(at(L.counts)), offsets,
+                           static_cast<int32_t*>(at(L.perm)), inv, at(L.x_perm), at(L.scratch), s)) != MOE_OK)
+      return st;
+  }
   const Split sp = choose_split(c, T, H, F, E, k);
   FfnOperands ops[2];
   ops[0] = FfnOperands{at(L.x_perm), offsets, Tk, E, H, F, w_gate, w_up, w_down, at(L.h_perm),
@@ -833,7 +842,7 @@ int moe_forward_launches(const moe_config_t* cfg, int T, int H, int F, int E, in
   else
     moe_config_default(&c);
   if (check_dims(T, H, F, E, k) != MOE_OK || check_config(c, H, E, k) != MOE_OK) return -1;
-  return forward_launches(c, T, H, E);
+  return forward_launches(c, T, H, E, k);
 }
 
 unsigned long long moe_launches_issued(void) { return moe::g_launch_count.load(std::memory_order_relaxed); }

@@ -265,9 +265,15 @@ __global__ void __launch_bounds__(kSmallThreads)
 
 }  // namespace
 
-bool permute_is_small(int T, int E) { return T <= kSmallT && E <= 256; }
+// The one-launch form repeats the bitmap work in every CTA and copies with
+// fewer threads in flight: measured on GB300 it wins up to about 2048 grouped
+// rows (Mixtral-shaped T=512: 10.5 vs 14 us) and loses above (4096 rows:
+// 29-35 vs 17-21 us).
+constexpr int kSmallRows = 2048;
 
-int permute_launches(int T, int E) { return T == 0 ? 0 : permute_is_small(T, E) ? 1 : 3; }
+bool permute_is_small(int T, int E, int k) { return T <= kSmallT && E <= 256 && T * k <= kSmallRows; }
+
+int permute_launches(int T, int E, int k) { return T == 0 ? 0 : permute_is_small(T, E, k) ? 1 : 3; }
 
 size_t permute_scratch_bytes(int T, int E) {
   const size_t W = (static_cast<size_t>(T) + 31) / 32;
@@ -277,7 +283,7 @@ size_t permute_scratch_bytes(int T, int E) {
 cudaError_t launch_permute(const int32_t* topk_idx, const void* x, int T, int H, int E, int k, int32_t* counts,
                            int32_t* offsets, int32_t* perm, int32_t* inv, void* x_perm, void* scratch,
                            uint32_t* err, cudaStream_t stream) {
-  if (permute_is_small(T, E)) {
+  if (permute_is_small(T, E, k)) {
     long long g = static_cast<long long>(T) * k;  // one CTA per copied row, up to 4 per SM
     if (g > 4 * 148) g = 4 * 148;
     if (g < 1) g = 1;

@@ -433,6 +433,129 @@ __global__ void shared_gate_kernel(const __nv_bfloat16* __restrict__ x, const __
   if (lane == 0) scale[warp] = 1.f / (1.f + __expf(-acc));
 }
 
+// Decode-sized batches (T <= kTinyT, router weights of at most kTinyWr
+// elements): routing and the grouping onto experts in one CTA, one launch.
+//  1. logits[t][e] = x[t] . W_r[e] (and x[t] . w_s for a gated shared
+//     expert): one warp per (token, expert) pair on the CUDA cores, fp32
+//     accumulation of the bf16 products, 16-byte loads;
+//  2. score, group limit and top-k by the same 8-lane team routine as
+//     router_kernel;
+//  3. counts, offsets (exclusive scan) and, for copy q = t*k + j of expert e,
+//     its grouped row offsets[e] + #{earlier tokens that chose e} (stable);
+//  4. perm, inv, and the x rows copied to x_perm.
+constexpr int kTinyT = 8;
+constexpr int kTinyWr = 128 * 1024;  // E * H
+constexpr int kTinyThreads = 256;
+
+struct TinyArgs {
+  RouterArgs r;
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* w_router;
+  const __nv_bfloat16* w_shared_gate;
+  int32_t *counts, *offsets, *perm, *inv;
+  uint4* x_perm;
+};
+
+__device__ __forceinline__ float dot_bf16_row(const __nv_bfloat16* a, const __nv_bfloat16* b, int H, int lane) {
+  const uint4* av = reinterpret_cast<const uint4*>(a);
+  const uint4* bv = reinterpret_cast<const uint4*>(b);
+  float acc = 0.f;
+  for (int v = lane; v < H / 8; v += 32) {
+    const uint4 xa = av[v], wa = bv[v];
+    const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&xa);
+    const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wa);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 xf = __bfloat1622float2(xp[i]), wf = __bfloat1622float2(wp[i]);
+      acc = fmaf(xf.x, wf.x, acc);
+      acc = fmaf(xf.y, wf.y, acc);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+  return acc;
+}
+
+__global__ void __launch_bounds__(kTinyThreads) route_permute_tiny_kernel(const TinyArgs ta) {
+  __shared__ float logits[(256 + 16) * kTinyT];  // column-major: logits[e * kTinyT + t]
+  __shared__ float bias_s[256];
+  __shared__ int32_t idx_s[kTinyT * 16];
+  __shared__ int32_t off_s[257];
+  pdl_trigger();
+  pdl_wait();
+  const RouterArgs& a = ta.r;
+  const int T = a.T, E = a.E, k = a.k, H = a.H;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ncol = E + (ta.w_shared_gate != nullptr ? 1 : 0);  // the gate is column E
+  for (int p = warp; p < T * ncol; p += kTinyThreads / 32) {
+    const int t = p / ncol, e = p - t * ncol;
+    const __nv_bfloat16* w = e < E ? ta.w_router + static_cast<size_t>(e) * H : ta.w_shared_gate;
+    const float v = dot_bf16_row(ta.x + static_cast<size_t>(t) * H, w, H, lane);
+    if (lane == 0) logits[e * kTinyT + t] = v;
+  }
+  if (a.spec.logit_bias != nullptr)
+    for (int e = threadIdx.x; e < E; e += kTinyThreads) bias_s[e] = a.spec.logit_bias[e];
+  __syncthreads();
+  // selection: team i of 8 lanes takes token i (the routine's gate column is column E)
+  {
+    const int team = threadIdx.x / kTeam, tl = threadIdx.x % kTeam;
+    if (warp < (T + 3) / 4) {  // warps holding at least one token's team
+      const bool active = team < T;
+      select_team(logits + (active ? team : 0), kTinyT, a.spec.logit_bias != nullptr ? bias_s : nullptr, a,
+                  team, tl, active);
+    }
+  }
+  __syncthreads();  // topk_idx written to global memory by the teams
+  for (int q = threadIdx.x; q < T * k; q += kTinyThreads) idx_s[q] = a.topk_idx[q];
+  __syncthreads();
+  // counts and offsets (E <= 256: thread e counts; a serial scan by thread 0)
+  if (threadIdx.x < E) {
+    int c = 0;
+    for (int q = 0; q < T * k; ++q) c += idx_s[q] == static_cast<int>(threadIdx.x);
+    off_s[threadIdx.x] = c;
+    ta.counts[threadIdx.x] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int e = 0; e < E; ++e) {
+      const int c = off_s[e];
+      off_s[e] = run;
+      run += c;
+    }
+    off_s[E] = run;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += kTinyThreads) ta.offsets[e] = off_s[e];
+  // grouped row of copy q: stable in token order
+  auto row_of = [&](int q) {
+    const int t = q / k, e = idx_s[q];
+    int r = off_s[e];
+    for (int q2 = 0; q2 < t * k; ++q2) r += idx_s[q2] == e;
+    return r;
+  };
+  for (int q = threadIdx.x; q < T * k; q += kTinyThreads) {
+    const int r = row_of(q);
+    ta.perm[r] = q;
+    ta.inv[q] = r;
+  }
+  const int H8 = H / 8;
+  for (int q = 0; q < T * k; ++q) {
+    const int r = row_of(q);  // the same for every thread
+    const uint4* src = reinterpret_cast<const uint4*>(ta.x + static_cast<size_t>(q / k) * H);
+    uint4* dst = ta.x_perm + static_cast<size_t>(r) * H8;
+    for (int v0 = threadIdx.x; v0 < H8; v0 += 4 * kTinyThreads) {
+      uint4 val[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v0 + u * kTinyThreads < H8) val[u] = src[v0 + u * kTinyThreads];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v0 + u * kTinyThreads < H8) dst[v0 + u * kTinyThreads] = val[u];
+    }
+  }
+}
+
 }  // namespace
 
 RouterPlan router_plan(int T, int H, int E, bool shared_gate) {
@@ -452,6 +575,36 @@ RouterPlan router_plan(int T, int H, int E, bool shared_gate) {
   p.kb_per_cta = (KB + c - 1) / c;
   p.cluster = c;
   return p;
+}
+
+bool route_permute_is_tiny(int T, int H, int E, int k) {
+  return T >= 1 && T <= kTinyT && static_cast<long long>(E) * H <= kTinyWr && E <= 256 && k <= 16;
+}
+
+cudaError_t launch_route_permute_tiny(int T, int H, int E, int k, const RouteSpec& spec, const void* x,
+                                      const void* w_router, const void* w_shared_gate, int32_t* topk_idx,
+                                      float* topk_w, float* shared_scale, int32_t* counts, int32_t* offsets,
+                                      int32_t* perm, int32_t* inv, void* x_perm, cudaStream_t stream) {
+  TinyArgs t{};
+  t.r.T = T;
+  t.r.H = H;
+  t.r.E = E;
+  t.r.k = k;
+  const bool gate = w_shared_gate != nullptr && shared_scale != nullptr;
+  t.r.gate_col = gate ? E : -1;
+  t.r.spec = spec;
+  t.r.topk_idx = topk_idx;
+  t.r.topk_w = topk_w;
+  t.r.shared_scale = shared_scale;
+  t.x = static_cast<const __nv_bfloat16*>(x);
+  t.w_router = static_cast<const __nv_bfloat16*>(w_router);
+  t.w_shared_gate = gate ? static_cast<const __nv_bfloat16*>(w_shared_gate) : nullptr;
+  t.counts = counts;
+  t.offsets = offsets;
+  t.perm = perm;
+  t.inv = inv;
+  t.x_perm = static_cast<uint4*>(x_perm);
+  return launch_kernel(route_permute_tiny_kernel, dim3(1), dim3(kTinyThreads), 0, stream, t);
 }
 
 int router_launches(int T, int H, int E, bool shared_gate) {

@@ -265,3 +265,20 @@ def test_forward_launch_count_matches_the_query(name, T, kw):
     moe.moe_forward_ex(d["x"][:T], d["w_router"], d["w_gate"], d["w_up"], d["w_down"], wl.k, cfg)
     assert moe.moe_launches_issued() - before == want > 0
     assert moe.moe_device_error()[0] == 0
+
+
+@pytest.mark.parametrize("name,T,alpha", [("skew", 1, 2.0), ("skew", 5, 2.0), ("skew", 8, 0.0), ("mixtral", 8, None),
+                                          ("tiny", 7, None)], ids=["skew-T1-a2", "skew-T5-a2", "skew-T8-a0",
+                                                                   "mixtral-T8", "tiny-T7"])
+def test_forward_decode_sizes_one_launch_routing(name, T, alpha):
+    """Decode-sized batches whose router weights are small route and group the
+    tokens in one launch (logits on the CUDA cores, the logit bias included):
+    routing, grouping and outputs against the oracle, and the launch count."""
+    wl, inp, d = _inputs(name, T, alpha)
+    cfg = make_cfg(wl, d)
+    before = moe.moe_launches_issued()
+    out = moe.moe_forward_ex(d["x"], d["w_router"], d["w_gate"], d["w_up"], d["w_down"], wl.k, cfg)
+    assert moe.moe_launches_issued() - before == moe.moe_forward_launches(cfg, T, wl.H, wl.F, wl.E, wl.k) == 4
+    assert moe.moe_device_error()[0] == 0
+    r = check_forward(wl, inp, d, out, cfg)
+    print(f"{wl.label}: rel-L2 {r['rel_l2']:.2e} max-abs {r['max_abs']:.2e}")
