@@ -131,7 +131,9 @@ cudaError_t launch_combine(const void* y_perm, const int32_t* inv, const float* 
   const dim3 grid((T + kWarpsPerBlock - 1) / kWarpsPerBlock, (H + 255) / 256);
   // Few warps (decode-sized batches): overlap the slice loads inside each
   // warp.  Many warps: one slice after the other (fewer registers, occupancy
-  // hides the latency), four expert rows in flight per warp.
+  // hides the latency), four expert rows in flight per warp (eight measured
+  // slower on GB300: DeepSeek-V3-shaped T=8192 260 -> 300 us, at lower
+  // occupancy).
   const long long warps = static_cast<long long>(T) * grid.y;
   void (*kernel)(const __half*, const int32_t*, const float*, const __half*, const float*, int, int, int,
                  __nv_bfloat16*, int, size_t, int, size_t) = combine_kernel<0, 0, 4>;

@@ -83,6 +83,7 @@ struct GemmArgs {
   int bn_max;
   int acc_cols;  // TMEM columns per accumulator slot: NSUB * bn_max
   int nslots;    // accumulator slots (2: the epilogue of a tile overlaps the next tile's MMAs)
+  int mix;       // spread segment 1's tiles evenly between segment 0's (see decode_tile)
   int tmem_cols;
   uint32_t* err;
 };
@@ -137,8 +138,28 @@ struct Tile {
   size_t out_off;  // element offset of this tile's output slice
 };
 
+// With two segments, position p of the tile sequence is a segment-1 tile
+// when floor((p + 1) n1 / n) > floor(p n1 / n) (n tiles, n1 of segment 1):
+// the shared expert's tiles (few weight bytes, all compute) are spread
+// evenly between the routed experts' tiles (weight streaming) instead of
+// running after them, so the weight stream and the tensor work overlap over
+// the whole launch.  Only when segment 1's token rows are small next to L2
+// (launch_grouped_gemm): measured on GB300, interleaving the Qwen2-shaped
+// shared expert (T=512, 3.7 MB of token rows) took its gate+up GEMM from 495
+// to 447 us, but interleaving the DeepSeek-V3-shaped one at T=8192 (117 MB
+// of token rows, re-read by every feature block) slowed it from 3600 to
+// 3790 us: its rows no longer stay in L2 between uses.
+#ifndef MOE_MIX_SEGMENTS
+#define MOE_MIX_SEGMENTS 1
+#endif
 __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const Sched& sc, int tile) {
   Tile t;
+  if (MOE_MIX_SEGMENTS && a.nseg > 1 && a.mix) {
+    const long long n = sc.seg_end[1], n1 = n - sc.seg_end[0];
+    const int c0 = static_cast<int>(static_cast<long long>(tile) * n1 / n);
+    const int c1 = static_cast<int>(static_cast<long long>(tile + 1) * n1 / n);
+    tile = c1 > c0 ? sc.seg_end[0] + c0 : tile - c0;
+  }
   t.s = (a.nseg > 1 && tile >= sc.seg_end[0]) ? 1 : 0;
   const SegDev& sg = a.seg[t.s];
   const int* pre = sc.prefix[t.s];
@@ -811,6 +832,7 @@ cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSe
   }
   a.acc_cols = plan.nsub * a.bn_max;
   a.nslots = 2 * a.acc_cols <= 512 ? 2 : 1;
+  a.mix = num_segments > 1 && static_cast<long long>(segs[1].rows) * segs[1].K * 2 <= (32ll << 20);
   a.tmem_cols = static_cast<int>(pow2_at_least(static_cast<uint32_t>(a.nslots * a.acc_cols)));
   a.kps = plan.kps;
   const int stage_bytes =

@@ -26,7 +26,11 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 192;  // warp 0: TMA, warp 1: MMA + TMEM owner, warps 2-5: TMEM -> shared memory
+// warp 0: TMA, warp 1: MMA + TMEM owner, warps 2-9: TMEM -> shared memory
+// (two column halves per TMEM lane quadrant); every warp takes part in the
+// reduction and the selection (48 teams of 8 lanes).
+constexpr int kThreads = 384;
+constexpr int kEpiWarps = 8;
 constexpr int kMaxStages = 8;
 constexpr int kMaxCluster = 8;
 constexpr int kTileM = 128;    // tokens per cluster
@@ -96,38 +100,62 @@ __device__ void select_team(const float* L, int ld, const float* bias, const Rou
   uint32_t kept = 0xFFFFFFFFu;
   if (ng > 1) {
     float gs_lo = -INFINITY, gs_hi = -INFINITY;
-    for (int g = 0; g < ng; ++g) {
-      float c[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // this lane's best four, descending
-      for (int e = g * gsize + tl; e < (g + 1) * gsize; e += kTeam) {
-        float v = logit(e), m;
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          m = fminf(c[j], v);
-          c[j] = fmaxf(c[j], v);
-          v = m;
+    const int n = a.spec.group_topn;
+    if (n <= 2) {
+      // top-2 per group: this lane's best two, then three butterfly merges of
+      // pairs; the group loop is unrolled so the merges of different groups
+      // overlap their shuffle latencies
+#pragma unroll 4
+      for (int g = 0; g < ng; ++g) {
+        float b1 = -INFINITY, b2 = -INFINITY;
+        for (int e = g * gsize + tl; e < (g + 1) * gsize; e += kTeam) {
+          const float v = logit(e);
+          b2 = fmaxf(b2, fminf(b1, v));
+          b1 = fmaxf(b1, v);
         }
-        c[3] = fmaxf(c[3], v);
+#pragma unroll
+        for (int o = kTeam / 2; o > 0; o >>= 1) {
+          const float p1 = __shfl_xor_sync(0xFFFFFFFFu, b1, o), p2 = __shfl_xor_sync(0xFFFFFFFFu, b2, o);
+          b2 = fmaxf(fminf(b1, p1), fmaxf(b2, p2));
+          b1 = fmaxf(b1, p1);
+        }
+        const float sg = score(b1) + (n > 1 ? score(b2) : 0.f);
+        if (g == tl) gs_lo = sg;
+        if (g == tl + kTeam) gs_hi = sg;
       }
-      // team merge: the best four of two descending lists (bitonic half
-      // cleaner, then a 4-element bitonic sort)
+    } else {
+      for (int g = 0; g < ng; ++g) {
+        float c[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // this lane's best four, descending
+        for (int e = g * gsize + tl; e < (g + 1) * gsize; e += kTeam) {
+          float v = logit(e), m;
 #pragma unroll
-      for (int o = kTeam / 2; o > 0; o >>= 1) {
-        float d[4];
+          for (int j = 0; j < 3; ++j) {
+            m = fminf(c[j], v);
+            c[j] = fmaxf(c[j], v);
+            v = m;
+          }
+          c[3] = fmaxf(c[3], v);
+        }
+        // team merge: the best four of two descending lists (bitonic half
+        // cleaner, then a 4-element bitonic sort)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) d[j] = fmaxf(c[j], __shfl_xor_sync(0xFFFFFFFFu, c[3 - j], o));
-        float x;
-        x = fmaxf(d[0], d[2]); d[2] = fminf(d[0], d[2]); d[0] = x;
-        x = fmaxf(d[1], d[3]); d[3] = fminf(d[1], d[3]); d[1] = x;
-        x = fmaxf(d[0], d[1]); d[1] = fminf(d[0], d[1]); d[0] = x;
-        x = fmaxf(d[2], d[3]); d[3] = fminf(d[2], d[3]); d[2] = x;
+        for (int o = kTeam / 2; o > 0; o >>= 1) {
+          float d[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) c[j] = d[j];
+          for (int j = 0; j < 4; ++j) d[j] = fmaxf(c[j], __shfl_xor_sync(0xFFFFFFFFu, c[3 - j], o));
+          float x;
+          x = fmaxf(d[0], d[2]); d[2] = fminf(d[0], d[2]); d[0] = x;
+          x = fmaxf(d[1], d[3]); d[3] = fminf(d[1], d[3]); d[1] = x;
+          x = fmaxf(d[0], d[1]); d[1] = fminf(d[0], d[1]); d[0] = x;
+          x = fmaxf(d[2], d[3]); d[3] = fminf(d[2], d[3]); d[2] = x;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) c[j] = d[j];
+        }
+        const float sg = score(c[0]) + (n > 1 ? score(c[1]) : 0.f) + (n > 2 ? score(c[2]) : 0.f) +
+                         (n > 3 ? score(c[3]) : 0.f);
+        if (g == tl) gs_lo = sg;
+        if (g == tl + kTeam) gs_hi = sg;
       }
-      const int n = a.spec.group_topn;
-      const float sg = score(c[0]) + (n > 1 ? score(c[1]) : 0.f) + (n > 2 ? score(c[2]) : 0.f) +
-                       (n > 3 ? score(c[3]) : 0.f);
-      if (g == tl) gs_lo = sg;
-      if (g == tl + kTeam) gs_hi = sg;
     }
     kept = 0;
     for (int r = 0; r < a.spec.topk_group; ++r) {
@@ -315,7 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // waited for their own accumulator), so every CTA's pipeline stages are free
   // to receive partial logits.
   bool acc_ok = true;
-  if (warp >= 2) {
+  const bool epi = warp >= 2 && warp < 2 + kEpiWarps;
+  if (epi) {
     acc_ok = mbar_wait(acc_full, 0, a.err, kSiteRouterEpilogue);
     acc_ok = __all_sync(0xFFFFFFFFu, acc_ok);  // the TMEM loads below are warp-collective
     tc_fence_after_sync();
@@ -328,24 +357,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rpc = kTileM / static_cast<int>(C);
   const int ld = logit_ld(static_cast<int>(C));
   const int slot_floats = a.NE * ld;
-  if (warp >= 2 && acc_ok) {
+  // Column halves: warps 2-5 take columns [0, NE/2), warps 6-9 [NE/2, NE)
+  // (NE a multiple of 64), else warps 2-5 take all columns.
+  const int halves = a.NE % 64 == 0 ? 2 : 1;
+  const int half = (warp - 2) / 4;
+  if (epi && acc_ok && half < halves) {
     const int q = warp & 3;
     const int row = q * 32 + lane;
+    const int cbeg = half * (a.NE / halves), cend = cbeg + a.NE / halves;
     const uint32_t owner = static_cast<uint32_t>(row / rpc);
     const int rr = row - static_cast<int>(owner) * rpc;  // row within the owner's share
     float* slot = P + static_cast<size_t>(rank) * slot_floats;
     const uint32_t dst = smem_u32(slot + rr);
     const bool local = owner == rank || C == 1;
     const uint32_t dst_c = local ? dst : mapa_shared(dst, owner);
-    for (int c0 = 0; c0 < a.NE; c0 += 32) {
+    for (int c0 = cbeg; c0 < cend; c0 += 32) {
       uint32_t r[32];
       const uint32_t ta = tmem_addr(tmem_base, q * 32, c0);
-      if (a.NE - c0 >= 32)
+      if (cend - c0 >= 32)
         tmem_ld32(ta, r);
       else
         tmem_ld16(ta, r);
       tmem_wait(r);
-      const int nc = min(32, a.NE - c0);
+      const int nc = min(32, cend - c0);
 #pragma unroll
       for (int i = 0; i < 32; ++i)
         if (i < nc) {
