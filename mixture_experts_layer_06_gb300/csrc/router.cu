@@ -57,19 +57,61 @@ __host__ __device__ constexpr int logit_ld(int C) { return kTileM / C + 4; }
 __host__ __device__ constexpr int logit_buffer_bytes(int NE, int C) { return C * NE * logit_ld(C) * 4 + 256 * 4; }
 
 constexpr int kTeam = 8;  // lanes that select the experts of one token
-constexpr int kMaxPerLane = 256 / kTeam;  // experts per lane (E <= 256)
 
 __device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
   return v1 > v2 || (v1 == v2 && i1 < i2);
 }
 
+// Team (8-lane butterfly) merges: the best two, or the best four in
+// descending order, of the values the lanes hold.
+__device__ __forceinline__ void team_top2(float& b1, float& b2) {
+#pragma unroll
+  for (int o = kTeam / 2; o > 0; o >>= 1) {
+    const float p1 = __shfl_xor_sync(0xFFFFFFFFu, b1, o), p2 = __shfl_xor_sync(0xFFFFFFFFu, b2, o);
+    b2 = fmaxf(fminf(b1, p1), fmaxf(b2, p2));
+    b1 = fmaxf(b1, p1);
+  }
+}
+__device__ __forceinline__ void team_top4(float (&c)[4]) {
+  // the best four of two descending lists: bitonic half cleaner, then a
+  // 4-element bitonic sort
+#pragma unroll
+  for (int o = kTeam / 2; o > 0; o >>= 1) {
+    float d[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) d[j] = fmaxf(c[j], __shfl_xor_sync(0xFFFFFFFFu, c[3 - j], o));
+    float x;
+    x = fmaxf(d[0], d[2]); d[2] = fminf(d[0], d[2]); d[0] = x;
+    x = fmaxf(d[1], d[3]); d[3] = fminf(d[1], d[3]); d[1] = x;
+    x = fmaxf(d[0], d[1]); d[1] = fminf(d[0], d[1]); d[0] = x;
+    x = fmaxf(d[2], d[3]); d[3] = fminf(d[2], d[3]); d[2] = x;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c[j] = d[j];
+  }
+}
+__device__ __forceinline__ void insert_top4(float (&c)[4], float v) {
+  float m;
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    m = fminf(c[j], v);
+    c[j] = fmaxf(c[j], v);
+    v = m;
+  }
+  c[3] = fmaxf(c[3], v);
+}
+
 // The k best experts of one token by a team of 8 lanes (tl = lane within the
 // team), from its summed logits L[e * ld] and the logit bias (both in shared
-// memory; bias may be null).  Lane tl looks at experts tl, tl + 8, ...  The
-// score functions are monotone, so experts (and a group's top scores) are
-// ranked by logit; scores are evaluated only where a value is needed.  Ties
-// go to the lower expert (group) index.  Every lane of the warp calls this
-// (the shuffles span the warp); only `active` teams write.
+// memory; bias may be null).  Lane tl holds the logits of experts tl + 8j,
+// j < JN (JN * 8 >= E), in registers, read once.  The score functions are
+// monotone, so experts (and a group's top scores) are ranked by logit; scores
+// are evaluated only where a value is needed.  Ties go to the lower expert
+// (group) index.  M > 0: the groups are E / n_group = 8M experts wide, so
+// group g is registers [gM, (g+1)M) of every lane and its best logits come
+// from registers; M = 0: any group width, read from shared memory.  Every
+// lane of the warp calls this (the shuffles span the warp); only `active`
+// teams write.
+template <int JN, int M>
 __device__ void select_team(const float* L, int ld, const float* bias, const RouterArgs& a, int t, int tl,
                             bool active) {
   const int E = a.E, k = a.k;
@@ -79,15 +121,24 @@ __device__ void select_team(const float* L, int ld, const float* bias, const Rou
   const int ng = a.spec.n_group > 1 ? a.spec.n_group : 1;
   const int gsize = E / ng;
 
+  float lv[JN];
+#pragma unroll
+  for (int j = 0; j < JN; ++j) {
+    const int e = tl + kTeam * j;
+    lv[j] = e < E ? logit(e) : -INFINITY;
+  }
+
   // Softmax normaliser over all E logits, when a softmax score is used
   // un-renormalised or inside a group score.
   float mx = -INFINITY, inv_se = 1.f;
   if (!sigmoid && (!a.spec.renormalize || ng > 1)) {
-    for (int e = tl; e < E; e += kTeam) mx = fmaxf(mx, logit(e));
+#pragma unroll
+    for (int j = 0; j < JN; ++j) mx = fmaxf(mx, lv[j]);
 #pragma unroll
     for (int o = kTeam / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
     float se = 0.f;
-    for (int e = tl; e < E; e += kTeam) se += __expf(logit(e) - mx);
+#pragma unroll
+    for (int j = 0; j < JN; ++j) se += __expf(lv[j] - mx);  // exp(-inf) = 0 past E
 #pragma unroll
     for (int o = kTeam / 2; o > 0; o >>= 1) se += __shfl_xor_sync(0xFFFFFFFFu, se, o);
     inv_se = 1.f / se;
@@ -97,67 +148,64 @@ __device__ void select_team(const float* L, int ld, const float* bias, const Rou
   // Group limit: group score = sum of the scores of its group_topn best
   // logits; the topk_group best groups are kept.  Lane tl holds the scores of
   // groups tl and tl + 8 (n_group <= 16).
-  uint32_t kept = 0xFFFFFFFFu;
   if (ng > 1) {
     float gs_lo = -INFINITY, gs_hi = -INFINITY;
     const int n = a.spec.group_topn;
-    if (n <= 2) {
-      // top-2 per group: this lane's best two, then three butterfly merges of
-      // pairs; the group loop is unrolled so the merges of different groups
-      // overlap their shuffle latencies
-#pragma unroll 4
-      for (int g = 0; g < ng; ++g) {
-        float b1 = -INFINITY, b2 = -INFINITY;
-        for (int e = g * gsize + tl; e < (g + 1) * gsize; e += kTeam) {
-          const float v = logit(e);
-          b2 = fmaxf(b2, fminf(b1, v));
-          b1 = fmaxf(b1, v);
-        }
+    if constexpr (M > 0) {
 #pragma unroll
-        for (int o = kTeam / 2; o > 0; o >>= 1) {
-          const float p1 = __shfl_xor_sync(0xFFFFFFFFu, b1, o), p2 = __shfl_xor_sync(0xFFFFFFFFu, b2, o);
-          b2 = fmaxf(fminf(b1, p1), fmaxf(b2, p2));
-          b1 = fmaxf(b1, p1);
+      for (int g = 0; g < JN / M; ++g) {
+        if (g < ng) {
+          float sg;
+          if (n <= 2) {
+            float b1 = -INFINITY, b2 = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < M; ++q) {
+              const float v = lv[g * M + q];
+              b2 = fmaxf(b2, fminf(b1, v));
+              b1 = fmaxf(b1, v);
+            }
+            team_top2(b1, b2);
+            sg = score(b1) + (n > 1 ? score(b2) : 0.f);
+          } else {
+            float c[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int q = 0; q < M; ++q) insert_top4(c, lv[g * M + q]);
+            team_top4(c);
+            sg = score(c[0]) + score(c[1]) + score(c[2]) + (n > 3 ? score(c[3]) : 0.f);
+          }
+          if (g == tl) gs_lo = sg;
+          if (g == tl + kTeam) gs_hi = sg;
         }
-        const float sg = score(b1) + (n > 1 ? score(b2) : 0.f);
-        if (g == tl) gs_lo = sg;
-        if (g == tl + kTeam) gs_hi = sg;
       }
     } else {
-      for (int g = 0; g < ng; ++g) {
-        float c[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // this lane's best four, descending
-        for (int e = g * gsize + tl; e < (g + 1) * gsize; e += kTeam) {
-          float v = logit(e), m;
-#pragma unroll
-          for (int j = 0; j < 3; ++j) {
-            m = fminf(c[j], v);
-            c[j] = fmaxf(c[j], v);
-            v = m;
+      if (n <= 2) {
+        // the group loop is unrolled so the merges of different groups
+        // overlap their shuffle latencies
+#pragma unroll 4
+        for (int g = 0; g < ng; ++g) {
+          float b1 = -INFINITY, b2 = -INFINITY;
+          for (int e = g * gsize + tl; e < (g + 1) * gsize; e += kTeam) {
+            const float v = logit(e);
+            b2 = fmaxf(b2, fminf(b1, v));
+            b1 = fmaxf(b1, v);
           }
-          c[3] = fmaxf(c[3], v);
+          team_top2(b1, b2);
+          const float sg = score(b1) + (n > 1 ? score(b2) : 0.f);
+          if (g == tl) gs_lo = sg;
+          if (g == tl + kTeam) gs_hi = sg;
         }
-        // team merge: the best four of two descending lists (bitonic half
-        // cleaner, then a 4-element bitonic sort)
-#pragma unroll
-        for (int o = kTeam / 2; o > 0; o >>= 1) {
-          float d[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) d[j] = fmaxf(c[j], __shfl_xor_sync(0xFFFFFFFFu, c[3 - j], o));
-          float x;
-          x = fmaxf(d[0], d[2]); d[2] = fminf(d[0], d[2]); d[0] = x;
-          x = fmaxf(d[1], d[3]); d[3] = fminf(d[1], d[3]); d[1] = x;
-          x = fmaxf(d[0], d[1]); d[1] = fminf(d[0], d[1]); d[0] = x;
-          x = fmaxf(d[2], d[3]); d[3] = fminf(d[2], d[3]); d[2] = x;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) c[j] = d[j];
+      } else {
+        for (int g = 0; g < ng; ++g) {
+          float c[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // this lane's best four, descending
+          for (int e = g * gsize + tl; e < (g + 1) * gsize; e += kTeam) insert_top4(c, logit(e));
+          team_top4(c);
+          const float sg = score(c[0]) + score(c[1]) + score(c[2]) + (n > 3 ? score(c[3]) : 0.f);
+          if (g == tl) gs_lo = sg;
+          if (g == tl + kTeam) gs_hi = sg;
         }
-        const float sg = score(c[0]) + (n > 1 ? score(c[1]) : 0.f) + (n > 2 ? score(c[2]) : 0.f) +
-                         (n > 3 ? score(c[3]) : 0.f);
-        if (g == tl) gs_lo = sg;
-        if (g == tl + kTeam) gs_hi = sg;
       }
     }
-    kept = 0;
+    uint32_t kept = 0;
     for (int r = 0; r < a.spec.topk_group; ++r) {
       // the best group not kept yet: this lane's candidate, then the team's
       const bool lo_ok = tl < ng && !((kept >> tl) & 1u), hi_ok = tl + kTeam < ng && !((kept >> (tl + kTeam)) & 1u);
@@ -178,45 +226,56 @@ __device__ void select_team(const float* L, int ld, const float* bias, const Rou
       }
       if (i != INT_MAX) kept |= 1u << i;
     }
-  }
-
-  // This lane's candidates (experts tl + 8j of the kept groups) in registers.
-  float lv[kMaxPerLane];
-  {
-    int g = 0, gend = gsize;
+    // only the experts of kept groups stay candidates
+    if constexpr (M > 0) {
 #pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j) {
-      const int e = tl + kTeam * j;
-      lv[j] = -INFINITY;
-      if (e < E) {
-        while (e >= gend) {
-          ++g;
-          gend += gsize;
+      for (int j = 0; j < JN; ++j)
+        if (!((kept >> (j / M)) & 1u)) lv[j] = -INFINITY;
+    } else {
+      int g = 0, gend = gsize;
+#pragma unroll
+      for (int j = 0; j < JN; ++j) {
+        const int e = tl + kTeam * j;
+        if (e < E) {
+          while (e >= gend) {
+            ++g;
+            gend += gsize;
+          }
+          if (!((kept >> g) & 1u)) lv[j] = -INFINITY;
         }
-        if ((kept >> g) & 1u) lv[j] = logit(e);
       }
     }
   }
 
-  // k rounds: each lane offers its best candidate not taken yet (the lowest
-  // j among equals: the lower expert id), the team's best wins the round and
-  // its lane marks it taken.  The weights are the scores of the k winners,
+  // k rounds: each lane offers its best remaining candidate (a tree arg-max
+  // over its registers, adjacent pairs first so that among equal logits the
+  // lower register -- the lower expert -- wins), the team's best wins the
+  // round and its lane drops it.  The weights are the scores of the k winners,
   // renormalised over them when asked (a renormalised softmax needs only the
   // winners' logits: its denominator cancels), times the routed scaling factor.
   const bool renorm_softmax = !sigmoid && a.spec.renormalize && ng == 1;
-  uint32_t taken = 0;
   float v0 = 0.f, sum = 0.f, s_lo = 0.f, s_hi = 0.f;
   int i_lo = -1, i_hi = -1;
   for (int r = 0; r < k; ++r) {
-    float v = -INFINITY;
-    int jb = -1;
+    float bv[JN];
+    int bj[JN];
 #pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j)
-      if (!((taken >> j) & 1u) && lv[j] != -INFINITY && (jb < 0 || lv[j] > v)) {
-        v = lv[j];
-        jb = j;
+    for (int j = 0; j < JN; ++j) {
+      bv[j] = lv[j];
+      bj[j] = j;
+    }
+#pragma unroll
+    for (int s = 1; s < JN; s <<= 1)
+#pragma unroll
+      for (int l = 0; l + s < JN; l += 2 * s) {
+        const bool right = bv[l + s] > bv[l];
+        bv[l] = right ? bv[l + s] : bv[l];
+        bj[l] = right ? bj[l + s] : bj[l];
       }
-    int i = jb >= 0 ? tl + kTeam * jb : INT_MAX;
+    float v = bv[0];
+    const int jb = bj[0];
+    const bool has = v != -INFINITY;
+    int i = has ? tl + kTeam * jb : INT_MAX;
     const int mine = i;
 #pragma unroll
     for (int o = kTeam / 2; o > 0; o >>= 1) {
@@ -227,7 +286,10 @@ __device__ void select_team(const float* L, int ld, const float* bias, const Rou
         i = i2;
       }
     }
-    if (jb >= 0 && i == mine) taken |= 1u << jb;
+    if (has && i == mine) {
+#pragma unroll
+      for (int j = 0; j < JN; ++j) lv[j] = j == jb ? -INFINITY : lv[j];
+    }
     if (r == 0) v0 = v;
     const float sc = renorm_softmax ? __expf(v - v0) : score(v);
     sum += sc;
@@ -249,6 +311,35 @@ __device__ void select_team(const float* L, int ld, const float* bias, const Rou
       a.topk_idx[static_cast<size_t>(t) * k + tl + kTeam] = i_hi;
       a.topk_w[static_cast<size_t>(t) * k + tl + kTeam] = s_hi * scale;
     }
+  }
+}
+
+// select_team with the register count JN for E and, where the groups line up
+// with the lanes' strides, the register-resident group layout.
+__device__ __forceinline__ void select_experts(const float* L, int ld, const float* bias, const RouterArgs& a, int t,
+                                               int tl, bool active) {
+  const int E = a.E;
+  const int ng = a.spec.n_group > 1 ? a.spec.n_group : 1;
+  const int m = (ng > 1 && (E / ng) % kTeam == 0) ? (E / ng) / kTeam : 0;
+  if (E > 16 * kTeam) {
+    if (m == 4)
+      select_team<32, 4>(L, ld, bias, a, t, tl, active);
+    else if (m == 2)
+      select_team<32, 2>(L, ld, bias, a, t, tl, active);
+    else if (m == 1)
+      select_team<32, 1>(L, ld, bias, a, t, tl, active);
+    else
+      select_team<32, 0>(L, ld, bias, a, t, tl, active);
+  } else if (E > 8 * kTeam) {
+    select_team<16, 0>(L, ld, bias, a, t, tl, active);
+  } else if (E > 4 * kTeam) {
+    select_team<8, 0>(L, ld, bias, a, t, tl, active);
+  } else if (E > 2 * kTeam) {
+    select_team<4, 0>(L, ld, bias, a, t, tl, active);
+  } else if (E > kTeam) {
+    select_team<2, 0>(L, ld, bias, a, t, tl, active);
+  } else {
+    select_team<1, 0>(L, ld, bias, a, t, tl, active);
   }
 }
 
@@ -431,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = base + team, t = m0 + static_cast<int>(rank) * rpc + r;
     const bool active = r < rpc && t < a.T;
     const float* L = P + (r < rpc ? r : 0);
-    select_team(L, ld, bias_s, a, t, tl, active);
+    select_experts(L, ld, bias_s, a, t, tl, active);
   }
   __syncthreads();
   if (warp == 1) {
@@ -510,7 +601,7 @@ __device__ __forceinline__ float dot_bf16_row(const __nv_bfloat16* a, const __nv
   return acc;
 }
 
-__global__ void __launch_bounds__(kTinyThreads) route_permute_tiny_kernel(const TinyArgs ta) {
+__global__ void __launch_bounds__(kTinyThreads, 1) route_permute_tiny_kernel(const TinyArgs ta) {
   __shared__ float logits[(256 + 16) * kTinyT];  // column-major: logits[e * kTinyT + t]
   __shared__ float bias_s[256];
   __shared__ int32_t idx_s[kTinyT * 16];
@@ -535,8 +626,8 @@ __global__ void __launch_bounds__(kTinyThreads) route_permute_tiny_kernel(const 
     const int team = threadIdx.x / kTeam, tl = threadIdx.x % kTeam;
     if (warp < (T + 3) / 4) {  // warps holding at least one token's team
       const bool active = team < T;
-      select_team(logits + (active ? team : 0), kTinyT, a.spec.logit_bias != nullptr ? bias_s : nullptr, a,
-                  team, tl, active);
+      select_experts(logits + (active ? team : 0), kTinyT, a.spec.logit_bias != nullptr ? bias_s : nullptr, a,
+                     team, tl, active);
     }
   }
   __syncthreads();  // topk_idx written to global memory by the teams
