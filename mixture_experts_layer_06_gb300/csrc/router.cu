@@ -100,6 +100,70 @@ __device__ __forceinline__ void insert_top4(float (&c)[4], float v) {
   c[3] = fmaxf(c[3], v);
 }
 
+// k rounds over a lane's NJ candidate logits lv[] (-inf = none; expert_of(j)
+// = the expert of register j, increasing in j): each lane offers its best
+// remaining candidate (a tree arg-max, adjacent pairs first so that among
+// equal logits the lower register -- the lower expert -- wins), the team's
+// best wins the round and its lane drops it.  The weights are the scores of
+// the k winners (renormalised softmax: exp(v - v0), the denominator cancels);
+// lane tl keeps rounds tl and tl + 8.
+struct RoundsOut {
+  float sum, s_lo, s_hi;
+  int i_lo, i_hi;
+};
+template <int NJ, typename ExpertOf, typename Score>
+__device__ __forceinline__ RoundsOut topk_rounds(float (&lv)[NJ], int k, int tl, bool renorm_softmax,
+                                                 ExpertOf expert_of, Score score) {
+  RoundsOut o{0.f, 0.f, 0.f, -1, -1};
+  float v0 = 0.f;
+  for (int r = 0; r < k; ++r) {
+    float bv[NJ];
+    int bj[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      bv[j] = lv[j];
+      bj[j] = j;
+    }
+#pragma unroll
+    for (int s = 1; s < NJ; s <<= 1)
+#pragma unroll
+      for (int l = 0; l + s < NJ; l += 2 * s) {
+        const bool right = bv[l + s] > bv[l];
+        bv[l] = right ? bv[l + s] : bv[l];
+        bj[l] = right ? bj[l + s] : bj[l];
+      }
+    float v = bv[0];
+    const int jb = bj[0];
+    const bool has = v != -INFINITY;
+    int i = has ? expert_of(jb) : INT_MAX;
+    const int mine = i;
+#pragma unroll
+    for (int off = kTeam / 2; off > 0; off >>= 1) {
+      const float v2 = __shfl_xor_sync(0xFFFFFFFFu, v, off);
+      const int i2 = __shfl_xor_sync(0xFFFFFFFFu, i, off);
+      if (better(v2, i2, v, i)) {
+        v = v2;
+        i = i2;
+      }
+    }
+    if (has && i == mine) {
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) lv[j] = j == jb ? -INFINITY : lv[j];
+    }
+    if (r == 0) v0 = v;
+    const float sc = renorm_softmax ? __expf(v - v0) : score(v);
+    o.sum += sc;
+    if (r == tl) {
+      o.s_lo = sc;
+      o.i_lo = i;
+    } else if (r == tl + kTeam) {
+      o.s_hi = sc;
+      o.i_hi = i;
+    }
+  }
+  return o;
+}
+
 // The k best experts of one token by a team of 8 lanes (tl = lane within the
 // team), from its summed logits L[e * ld] and the logit bias (both in shared
 // memory; bias may be null).  Lane tl holds the logits of experts tl + 8j,
@@ -148,6 +212,7 @@ __device__ void select_team(const float* L, int ld, const float* bias, const Rou
   // Group limit: group score = sum of the scores of its group_topn best
   // logits; the topk_group best groups are kept.  Lane tl holds the scores of
   // groups tl and tl + 8 (n_group <= 16).
+  uint32_t kept = 0xFFFFFFFFu;
   if (ng > 1) {
     float gs_lo = -INFINITY, gs_hi = -INFINITY;
     const int n = a.spec.group_topn;
@@ -205,7 +270,7 @@ __device__ void select_team(const float* L, int ld, const float* bias, const Rou
         }
       }
     }
-    uint32_t kept = 0;
+    kept = 0;
     for (int r = 0; r < a.spec.topk_group; ++r) {
       // the best group not kept yet: this lane's candidate, then the team's
       const bool lo_ok = tl < ng && !((kept >> tl) & 1u), hi_ok = tl + kTeam < ng && !((kept >> (tl + kTeam)) & 1u);
@@ -247,69 +312,50 @@ __device__ void select_team(const float* L, int ld, const float* bias, const Rou
     }
   }
 
-  // k rounds: each lane offers its best remaining candidate (a tree arg-max
-  // over its registers, adjacent pairs first so that among equal logits the
-  // lower register -- the lower expert -- wins), the team's best wins the
-  // round and its lane drops it.  The weights are the scores of the k winners,
-  // renormalised over them when asked (a renormalised softmax needs only the
-  // winners' logits: its denominator cancels), times the routed scaling factor.
   const bool renorm_softmax = !sigmoid && a.spec.renormalize && ng == 1;
-  float v0 = 0.f, sum = 0.f, s_lo = 0.f, s_hi = 0.f;
-  int i_lo = -1, i_hi = -1;
-  for (int r = 0; r < k; ++r) {
-    float bv[JN];
-    int bj[JN];
+  RoundsOut o;
+  if constexpr (M > 0) {
+    if (ng > 1 && a.spec.topk_group * M <= JN / 2) {
+      // The kept groups' candidates, compacted into half the registers (slot
+      // s = the s-th kept group in ascending order, so register order still
+      // follows expert order); the rounds then scan half as many values.
+      constexpr int CJ = JN / 2, NS = CJ / M;
+      float cv[CJ];
+      unsigned long long gpack = 0;  // 4 bits per slot: its group (n_group <= 16)
+      uint32_t rem = kept;
 #pragma unroll
-    for (int j = 0; j < JN; ++j) {
-      bv[j] = lv[j];
-      bj[j] = j;
-    }
+      for (int sl = 0; sl < NS; ++sl) {
+        const int g = rem != 0 ? __ffs(rem) - 1 : -1;
+        rem &= rem - 1;
+        gpack |= static_cast<unsigned long long>(g & 15) << (4 * sl);
 #pragma unroll
-    for (int s = 1; s < JN; s <<= 1)
+        for (int q = 0; q < M; ++q) {
+          float v = -INFINITY;
 #pragma unroll
-      for (int l = 0; l + s < JN; l += 2 * s) {
-        const bool right = bv[l + s] > bv[l];
-        bv[l] = right ? bv[l + s] : bv[l];
-        bj[l] = right ? bj[l + s] : bj[l];
+          for (int g2 = 0; g2 < JN / M; ++g2) v = g == g2 ? lv[g2 * M + q] : v;
+          cv[sl * M + q] = v;
+        }
       }
-    float v = bv[0];
-    const int jb = bj[0];
-    const bool has = v != -INFINITY;
-    int i = has ? tl + kTeam * jb : INT_MAX;
-    const int mine = i;
-#pragma unroll
-    for (int o = kTeam / 2; o > 0; o >>= 1) {
-      const float v2 = __shfl_xor_sync(0xFFFFFFFFu, v, o);
-      const int i2 = __shfl_xor_sync(0xFFFFFFFFu, i, o);
-      if (better(v2, i2, v, i)) {
-        v = v2;
-        i = i2;
-      }
+      auto expert_of = [gpack, gsize, tl](int j) {
+        const int g = static_cast<int>((gpack >> (4 * (j / M))) & 15u);
+        return g * gsize + tl + kTeam * (j % M);
+      };
+      o = topk_rounds(cv, k, tl, renorm_softmax, expert_of, score);
+    } else {
+      o = topk_rounds(lv, k, tl, renorm_softmax, [tl](int j) { return tl + kTeam * j; }, score);
     }
-    if (has && i == mine) {
-#pragma unroll
-      for (int j = 0; j < JN; ++j) lv[j] = j == jb ? -INFINITY : lv[j];
-    }
-    if (r == 0) v0 = v;
-    const float sc = renorm_softmax ? __expf(v - v0) : score(v);
-    sum += sc;
-    if (r == tl) {
-      s_lo = sc;
-      i_lo = i;
-    } else if (r == tl + kTeam) {
-      s_hi = sc;
-      i_hi = i;
-    }
+  } else {
+    o = topk_rounds(lv, k, tl, renorm_softmax, [tl](int j) { return tl + kTeam * j; }, score);
   }
-  const float scale = a.spec.renormalize ? a.spec.route_scale / sum : a.spec.route_scale;
+  const float scale = a.spec.renormalize ? a.spec.route_scale / o.sum : a.spec.route_scale;
   if (active) {
     if (tl < k) {
-      a.topk_idx[static_cast<size_t>(t) * k + tl] = i_lo;
-      a.topk_w[static_cast<size_t>(t) * k + tl] = s_lo * scale;
+      a.topk_idx[static_cast<size_t>(t) * k + tl] = o.i_lo;
+      a.topk_w[static_cast<size_t>(t) * k + tl] = o.s_lo * scale;
     }
     if (tl + kTeam < k) {
-      a.topk_idx[static_cast<size_t>(t) * k + tl + kTeam] = i_hi;
-      a.topk_w[static_cast<size_t>(t) * k + tl + kTeam] = s_hi * scale;
+      a.topk_idx[static_cast<size_t>(t) * k + tl + kTeam] = o.i_hi;
+      a.topk_w[static_cast<size_t>(t) * k + tl + kTeam] = o.s_hi * scale;
     }
   }
 }
