@@ -73,11 +73,14 @@ struct RouteSpec {
 
 // Router launch plan: logit columns NE (E rounded up to 16, plus 16 when the
 // shared-expert gate vector rides along as one more B row), and the K split:
-// a cluster of `cluster` CTAs per 128-token tile, each reducing kb_per_cta
-// 64-wide K blocks.  Shapes only.
+// ksplit CTAs (or CTA pairs, `pair`) per token tile of 128 (256) tokens, each
+// reducing kb_per_cta 64-wide K blocks; a cluster of `cluster` CTAs per tile.
+// With pairs, map_wr's box is NE/2 rows.  Shapes only.
 struct RouterPlan {
   bool fused_gate;
+  bool pair;
   int NE;
+  int ksplit;
   int cluster;
   int kb_per_cta;
   int m_tiles;
@@ -88,8 +91,8 @@ RouterPlan router_plan(int T, int H, int E, bool shared_gate);
 // cores, partial logits of the cluster added over distributed shared memory,
 // then score, group limit and top-k per token), plus the separate shared-gate
 // kernel when the gate row does not fit.  map_x: box {64, 128}; map_wr: [E, H]
-// box {64, E rounded up to 16}; map_ws: [1, H] box {64, 16} (used when the
-// plan fuses the gate).
+// box {64, E rounded up to 16}, halved when router_plan pairs the CTAs;
+// map_ws: [1, H] box {64, 16} (used when the plan fuses the gate).
 cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_wr, const CUtensorMap* map_ws, int T,
                           int H, int E, int k, const RouteSpec& spec, const void* x, const void* w_shared_gate,
                           int32_t* topk_idx, float* topk_w, float* shared_scale, uint32_t* err,

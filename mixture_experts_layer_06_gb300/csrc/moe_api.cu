@@ -348,8 +348,11 @@ Layout layout(const moe_config_t& c, int T, int H, int F, int E, int k) {
 moe_status_t route_impl(DeviceState* d, const moe_config_t& c, const void* x, const void* w_router, int T, int H,
                         int E, int k, int32_t* topk_idx, float* topk_w, float* shared_scale, cudaStream_t stream) {
   CUtensorMap mx, mw, ms;
-  if (!make_map(&mx, x, T, H, 128) || !make_map(&mw, w_router, E, H, (E + 15) / 16 * 16)) return MOE_ERR_CUDA;
   const bool gate = c.w_shared_gate != nullptr && shared_scale != nullptr;
+  const moe::RouterPlan plan = moe::router_plan(T, H, E, gate);
+  const uint32_t wr_rows = (E + 15) / 16 * 16;
+  if (!make_map(&mx, x, T, H, 128) || !make_map(&mw, w_router, E, H, plan.pair ? wr_rows / 2 : wr_rows))
+    return MOE_ERR_CUDA;
   if (gate && !make_map(&ms, c.w_shared_gate, 1, H, 16)) return MOE_ERR_CUDA;
   const cudaError_t e = moe::launch_router(mx, mw, gate ? &ms : nullptr, T, H, E, k, route_spec(c), x,
                                            gate ? c.w_shared_gate : nullptr, topk_idx, topk_w,

@@ -340,12 +340,15 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc,
 }
 
 // Arrive once on `bar` (same shared-memory offset) in both CTAs of the pair
-// when the pair's prior tcgen05 operations complete.
-__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+// when the pair's prior tcgen05 operations complete.  umma_commit_pair: the
+// pair is cluster ranks 0 and 1; umma_commit_pair_at: the pair whose even
+// CTA is cluster rank `even`.
+__device__ __forceinline__ void umma_commit_pair_at(uint64_t* bar, uint32_t even) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-      ::"r"(smem_u32(bar)), "h"(static_cast<uint16_t>(3))
+      ::"r"(smem_u32(bar)), "h"(static_cast<uint16_t>(3u << even))
       : "memory");
 }
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) { umma_commit_pair_at(bar, 0); }
 
 }  // namespace moe

@@ -7,7 +7,11 @@
 // router_kernel: a cluster of C CTAs per tile of 128 tokens.  CTA r of the
 // cluster computes the partial logits x . [W_r; w_s]^T over its share of the
 // K = H columns on the 5th-generation tensor cores (tcgen05.mma, operands
-// staged by TMA, fp32 accumulator in TMEM).  CTA r owns tokens
+// staged by TMA, fp32 accumulator in TMEM).  Large batches with a wide router
+// run as C CTA pairs per tile of 256 tokens instead (cta_group::2: each CTA
+// of a pair holds 128 token rows and half of the W_r rows, so every CTA
+// streams half as many W_r bytes per token); everything below then happens
+// within each half of the pairs.  CTA r owns tokens
 // [r*128/C, (r+1)*128/C) of the tile: every CTA stores its partial logits of
 // a token into the owner's shared memory (distributed shared memory stores,
 // slot = source rank, column-major so that a warp's stores are contiguous),
@@ -33,6 +37,7 @@ constexpr int kThreads = 384;
 constexpr int kEpiWarps = 8;
 constexpr int kMaxStages = 8;
 constexpr int kMaxCluster = 8;
+constexpr int kPairMinT = 4096;  // batches from which the router runs as CTA pairs (router_plan)
 constexpr int kTileM = 128;    // tokens per cluster
 constexpr int kTileK = 64;     // bf16 elements per 128-byte swizzled row
 constexpr int kATileBytes = kTileM * kTileK * 2;
@@ -389,14 +394,20 @@ __device__ __forceinline__ void select_experts(const float* L, int ld, const flo
   }
 }
 
+// PAIR: the CTAs run as pairs (tcgen05 cta_group::2; one kernel may not mix
+// the two CTA granularities).
+template <bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     router_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_wr,
                   const __grid_constant__ CUtensorMap map_ws, const RouterArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages;
-  const int stage_bytes = kATileBytes + a.NE * kTileK * 2;
-  const uint32_t C = gridDim.x;  // cluster size: the cluster spans blockIdx.x
+  constexpr bool pair = PAIR;
+  // B rows per CTA: all NE, or half of them on each CTA of a pair
+  const int stage_bytes = kATileBytes + (pair ? a.NE / 2 : a.NE) * kTileK * 2;
+  const uint32_t CL = gridDim.x;         // cluster size: the cluster spans blockIdx.x
+  const uint32_t C = pair ? CL / 2 : CL;  // CTAs (pairs) splitting K
   const int region = max(S * stage_bytes, logit_buffer_bytes(a.NE, static_cast<int>(C)));
   float* P = reinterpret_cast<float*>(smem);  // summed / partial logits, after the last MMA
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + region);
@@ -405,10 +416,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = C > 1 ? cluster_ctarank() : 0;
-  const int m0 = blockIdx.y * kTileM;
+  const uint32_t rank = CL > 1 ? cluster_ctarank() : 0;
+  const uint32_t kr = pair ? rank >> 1 : rank;  // K share
+  const uint32_t phalf = pair ? rank & 1 : 0;   // a pair's CTA: token rows [128 phalf, +128) of the pair's 256
+  const uint32_t even = rank & ~1u;             // the pair's even CTA (cluster rank)
+  const int m0 = blockIdx.y * (pair ? 2 * kTileM : kTileM) + static_cast<int>(phalf) * kTileM;
   const int KB = a.H / kTileK;
-  const int kb0 = static_cast<int>(rank) * a.kb_per_cta;
+  const int kb0 = static_cast<int>(kr) * a.kb_per_cta;
   const int kb1 = min(KB, kb0 + a.kb_per_cta);
   const int nboxes = a.n_wr_boxes + (a.gate_box >= 0 ? 1 : 0);
 
@@ -426,51 +440,91 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, a.tmem_cols);
-    tmem_relinquish();
+    if (pair) {
+      tmem_alloc_pair(tmem_holder, a.tmem_cols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_holder, a.tmem_cols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
+  if (pair) cluster_sync();  // the pair's barriers exist before any remote use
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_holder;
 
   if (warp == 0) {
     // Lane 0: wait for the slot, post the bytes, load the x tile, the W_r rows
     // (one box) and, with a fused gate, the w_s row (one 16-row box).
+    // A pair: each CTA loads its 128 token rows and its half of the W_r rows
+    // (map_wr's box is NE/2 rows), both completing on the even CTA's barrier.
     if (lane == 0) {
       int issued = 0;
+      int s = 0;         // ring slot and phase of stage `issued` (running counters)
+      uint32_t ph = 0;
       for (int kb = kb0; kb < kb1; ++kb, ++issued) {
-        const int s = issued % S;
-        const uint32_t ph = (issued / S) & 1;
         if (!mbar_wait(&empty[s], ph ^ 1, a.err, kSiteRouterProducer)) break;
-        mbar_arrive_expect_tx(&full[s], kATileBytes + nboxes * kBoxBytes);
         uint8_t* st = smem + s * stage_bytes;
-        tma_load_2d(st, &map_x, &full[s], kb * kTileK, m0);
-        tma_load_2d(st + kATileBytes, &map_wr, &full[s], kb * kTileK, 0);
-        if (a.gate_box >= 0) tma_load_2d(st + kATileBytes + a.gate_box * kBoxBytes, &map_ws, &full[s], kb * kTileK, 0);
+        if (pair) {
+          if (phalf == 0) mbar_arrive_expect_tx(&full[s], 2u * static_cast<uint32_t>(stage_bytes));
+          const uint32_t bar = mapa_shared(smem_u32(&full[s]), even);
+          tma_load_2d_pair(st, &map_x, bar, kb * kTileK, m0);
+          tma_load_2d_pair(st + kATileBytes, &map_wr, bar, kb * kTileK, static_cast<int>(phalf) * (a.NE / 2));
+        } else {
+          mbar_arrive_expect_tx(&full[s], kATileBytes + nboxes * kBoxBytes);
+          tma_load_2d(st, &map_x, &full[s], kb * kTileK, m0);
+          tma_load_2d(st + kATileBytes, &map_wr, &full[s], kb * kTileK, 0);
+          if (a.gate_box >= 0)
+            tma_load_2d(st + kATileBytes + a.gate_box * kBoxBytes, &map_ws, &full[s], kb * kTileK, 0);
+        }
+        if (++s == S) {
+          s = 0;
+          ph ^= 1;
+        }
       }
-      // Do not leave while copies into this CTA's shared memory are in flight.
-      for (int i = (issued > S ? issued - S : 0); i < issued; ++i)
-        mbar_wait(&full[i % S], (i / S) & 1, a.err, kSiteTeardown);
+      // Do not leave while copies into this CTA's shared memory are in flight
+      // (a pair's loads complete on the even CTA: wait until they were consumed).
+      for (int i = (issued > S ? issued - S : 0); i < issued; ++i) {
+        if (pair)
+          mbar_wait(&empty[i % S], (i / S) & 1, a.err, kSiteTeardown);
+        else
+          mbar_wait(&full[i % S], (i / S) & 1, a.err, kSiteTeardown);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kTileM, a.NE);
-      int n = 0;
-      for (int kb = kb0; kb < kb1; ++kb, ++n) {
-        const int s = n % S;
-        if (!mbar_wait(&full[s], (n / S) & 1, a.err, kSiteRouterMma)) break;
+    if (lane == 0 && phalf == 0) {  // a pair's MMAs are issued by its even CTA
+      const uint32_t idesc = idesc_bf16_f32(pair ? 2 * kTileM : kTileM, a.NE);
+      int s = 0;
+      uint32_t ph = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&full[s], ph, a.err, kSiteRouterMma)) break;
         tc_fence_after_sync();
         const uint32_t a_addr = smem_u32(smem + s * stage_bytes);
         const uint32_t b_addr = a_addr + kATileBytes;
 #pragma unroll
-        for (int kk = 0; kk < kTileK / 16; ++kk)
-          umma_bf16(tmem_base, sdesc_k128(a_addr + kk * 32), sdesc_k128(b_addr + kk * 32), idesc,
-                    (kb != kb0 || kk != 0));
-        umma_commit(&empty[s]);
+        for (int kk = 0; kk < kTileK / 16; ++kk) {
+          if (pair)
+            umma_bf16_pair(tmem_base, sdesc_k128(a_addr + kk * 32), sdesc_k128(b_addr + kk * 32), idesc,
+                           (kb != kb0 || kk != 0));
+          else
+            umma_bf16(tmem_base, sdesc_k128(a_addr + kk * 32), sdesc_k128(b_addr + kk * 32), idesc,
+                      (kb != kb0 || kk != 0));
+        }
+        if (pair)
+          umma_commit_pair_at(&empty[s], even);
+        else
+          umma_commit(&empty[s]);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1;
+        }
       }
-      umma_commit(acc_full);
+      if (pair)
+        umma_commit_pair_at(acc_full, even);
+      else
+        umma_commit(acc_full);
     }
     __syncwarp();
   }
@@ -487,10 +541,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
   }
   __syncthreads();
-  if (C > 1) cluster_sync();
+  if (CL > 1) cluster_sync();
 
   // Thread = token row (TMEM lane): its NE partial logits go to the CTA that
-  // owns the row, into slot `rank` of that CTA's buffer R[C][NE][ld].
+  // owns the row, into slot `kr` of that CTA's buffer R[C][NE][ld] (with
+  // pairs: the CTA of the same pair half in the owning pair).
   const int rpc = kTileM / static_cast<int>(C);
   const int ld = logit_ld(static_cast<int>(C));
   const int slot_floats = a.NE * ld;
@@ -502,12 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const int cbeg = half * (a.NE / halves), cend = cbeg + a.NE / halves;
-    const uint32_t owner = static_cast<uint32_t>(row / rpc);
+    const uint32_t owner = static_cast<uint32_t>(row / rpc);  // its K share index
     const int rr = row - static_cast<int>(owner) * rpc;  // row within the owner's share
-    float* slot = P + static_cast<size_t>(rank) * slot_floats;
+    float* slot = P + static_cast<size_t>(kr) * slot_floats;
     const uint32_t dst = smem_u32(slot + rr);
-    const bool local = owner == rank || C == 1;
-    const uint32_t dst_c = local ? dst : mapa_shared(dst, owner);
+    const bool local = owner == kr || C == 1;
+    const uint32_t dst_c = local ? dst : mapa_shared(dst, pair ? 2 * owner + phalf : owner);
     for (int c0 = cbeg; c0 < cend; c0 += 32) {
       uint32_t r[32];
       const uint32_t ta = tmem_addr(tmem_base, q * 32, c0);
@@ -532,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Barrier 2: every partial row has arrived.  After it no CTA touches
   // another's shared memory.
   __syncthreads();
-  if (C > 1) cluster_sync();
+  if (CL > 1) cluster_sync();
 
   // Owned rows: add the C partials in rank order into slot 0.
   if (C > 1) {
@@ -565,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int team = threadIdx.x / kTeam, tl = threadIdx.x % kTeam;
   for (int base = 0; base < rpc; base += kTeams) {
     if (base + (threadIdx.x & ~31) / kTeam >= rpc) break;  // whole warp past the owned rows
-    const int r = base + team, t = m0 + static_cast<int>(rank) * rpc + r;
+    const int r = base + team, t = m0 + static_cast<int>(kr) * rpc + r;
     const bool active = r < rpc && t < a.T;
     const float* L = P + (r < rpc ? r : 0);
     select_experts(L, ld, bias_s, a, t, tl, active);
@@ -573,7 +628,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, a.tmem_cols);
+    if (pair)
+      tmem_dealloc_pair(tmem_base, a.tmem_cols);
+    else
+      tmem_dealloc(tmem_base, a.tmem_cols);
   }
 }
 
@@ -734,17 +792,26 @@ RouterPlan router_plan(int T, int H, int E, bool shared_gate) {
   const int ne_wr = (E + 15) / 16 * 16;
   p.fused_gate = shared_gate && ne_wr + 16 <= 256;
   p.NE = ne_wr + (p.fused_gate ? 16 : 0);
-  p.m_tiles = (T + kTileM - 1) / kTileM;
+  // CTA pairs for large batches with a wide router: every 128-token tile
+  // re-reads all of W_r from L2, and a pair (M = 256 tokens per MMA) halves
+  // that; each CTA of a pair holds half of the NE rows of B, so the fused
+  // shared-expert gate row, which must sit with the W_r rows, is not paired.
+  p.pair = !p.fused_gate && p.NE >= 128 && T >= kPairMinT;
+  const int rows = p.pair ? 2 * kTileM : kTileM;
+  p.m_tiles = (T + rows - 1) / rows;
   const int KB = H / kTileK;
-  // The largest power-of-two cluster (<= 8) that keeps the grid within one
-  // wave of ~152 CTAs and leaves every CTA at least two K blocks, so that the
-  // W_r stream of a small batch spreads over several SMs.  Shapes only.
+  // The largest power-of-two K split c (a cluster of c CTAs, or c pairs;
+  // at most 8 CTAs) that keeps the grid within one wave of ~152 CTAs and
+  // leaves every CTA at least two K blocks, so that the W_r stream of a small
+  // batch spreads over several SMs.  Shapes only.
+  const int per = p.pair ? 2 : 1;
   int c = 1;
-  while (c < kMaxCluster && p.m_tiles * (2 * c) <= 152 && KB / (2 * c) >= 2) c <<= 1;
+  while (per * c < kMaxCluster && p.m_tiles * per * (2 * c) <= 152 && KB / (2 * c) >= 2) c <<= 1;
   p.kb_per_cta = (KB + c - 1) / c;
   while (c > 1 && (c - 1) * p.kb_per_cta >= KB) c >>= 1;  // every CTA gets a K block
   p.kb_per_cta = (KB + c - 1) / c;
-  p.cluster = c;
+  p.ksplit = c;
+  p.cluster = per * c;
   return p;
 }
 
@@ -807,13 +874,13 @@ cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_wr, c
   g.topk_w = topk_w;
   g.shared_scale = shared_scale;
   g.err = err;
-  const int stage_bytes = kATileBytes + p.NE * kTileK * 2;
+  const int stage_bytes = kATileBytes + (p.pair ? p.NE / 2 : p.NE) * kTileK * 2;
   const int fixed = 1024 + (2 * kMaxStages + 2) * 8 + 64;
   int stages = (227 * 1024 - fixed) / stage_bytes;
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages > p.kb_per_cta) stages = p.kb_per_cta;
   g.stages = stages;
-  const int lbuf = logit_buffer_bytes(p.NE, p.cluster);
+  const int lbuf = logit_buffer_bytes(p.NE, p.ksplit);
   const int region = stages * stage_bytes > lbuf ? stages * stage_bytes : lbuf;
   // At least half an SM's shared memory, so that one router CTA at most runs
   // on an SM: a CTA that waits at a cluster barrier then never holds TMEM
@@ -821,16 +888,17 @@ cudaError_t launch_router(const CUtensorMap& map_x, const CUtensorMap& map_wr, c
   size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(region);
   if (smem < 116 * 1024) smem = 116 * 1024;
 
-  static bool configured[64] = {};
+  static bool configured[2][64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  auto kernel = p.pair ? router_kernel<true> : router_kernel<false>;
+  if (dev < 64 && !configured[p.pair][dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[p.pair][dev] = true;
   }
   const dim3 grid(p.cluster, p.m_tiles);
-  cudaError_t e = launch_kernel_cluster(router_kernel, grid, dim3(kThreads), smem, stream, p.cluster, map_x, map_wr,
+  cudaError_t e = launch_kernel_cluster(kernel, grid, dim3(kThreads), smem, stream, p.cluster, map_x, map_wr,
                                         p.fused_gate ? *map_ws : map_wr, g);
   if (e != cudaSuccess) return e;
   if (gate && !p.fused_gate) {

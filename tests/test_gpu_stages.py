@@ -37,6 +37,10 @@ ROUTER_CASES = [
     # top-3 / top-1 per group, 16 groups of 16
     ("deepseek", 256, {"E": 64}), ("deepseek", 256, {"group_topn": 3}), ("deepseek", 256, {"group_topn": 1}),
     ("deepseek", 256, {"n_group": 16, "topk_group": 6}),
+    # batches that run the router as CTA pairs (256 tokens per MMA, half of
+    # W_r on each CTA): a ragged last pair tile, and 144 experts (72 W_r rows
+    # per CTA) without groups
+    ("deepseek", 4100, {}), ("deepseek", 4096, {"E": 144, "n_group": 1, "topk_group": 1, "group_topn": 0}),
 ]
 
 
