@@ -72,6 +72,7 @@ struct SegDev {
   int gelu;      // gated epilogue: GELU (erf form) instead of SiLU
   size_t slice_stride;
   void* out;
+  int kstages;   // stages of kps K blocks in the full K
 };
 
 struct GemmArgs {
@@ -91,7 +92,7 @@ struct GemmArgs {
 struct Sched {
   int prefix[2][kMaxSegGroups + 1];    // first tile of each group
   int rowstart[2][kMaxSegGroups + 1];  // first B row of each group; [G] = end
-  int trows[2][kMaxSegGroups];         // token rows per tile of each group
+  int trows[2][kMaxSegGroups];         // token rows per tile of each group | token tiles << 10
   int seg_end[2];                      // tile count after segment 0 / 1
 };
 
@@ -152,7 +153,15 @@ struct Tile {
 #ifndef MOE_MIX_SEGMENTS
 #define MOE_MIX_SEGMENTS 1
 #endif
-__device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const Sched& sc, int tile) {
+// A role's place in its walk over the tiles: the group of the last tile it
+// decoded in each segment.  A role visits its tiles in increasing order, and
+// so (also with segments mixed) increasing within each segment, so the group
+// of the next tile is found by scanning forward from there.
+struct WalkHint {
+  int g0, g1;  // segment 0, segment 1 (two scalars: an indexed pair would live in local memory)
+};
+
+__device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const Sched& sc, int tile, WalkHint& h) {
   Tile t;
   if (MOE_MIX_SEGMENTS && a.nseg > 1 && a.mix) {
     const long long n = sc.seg_end[1], n1 = n - sc.seg_end[0];
@@ -163,30 +172,41 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const Sched& sc, 
   t.s = (a.nseg > 1 && tile >= sc.seg_end[0]) ? 1 : 0;
   const SegDev& sg = a.seg[t.s];
   const int* pre = sc.prefix[t.s];
-  int lo = 0, hi = sg.groups - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (pre[mid] <= tile)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  t.g = lo;
-  int local = tile - pre[lo];
-  const int rows_g = sc.rowstart[t.s][lo + 1] - sc.rowstart[t.s][lo];
+  int g = t.s ? h.g1 : h.g0;  // the last group with pre[g] <= tile (empty groups are passed over)
+  while (g + 1 < sg.groups && pre[g + 1] <= tile) ++g;
+  if (t.s)
+    h.g1 = g;
+  else
+    h.g0 = g;
+  t.g = g;
+  int local = tile - pre[g];
+  const int rows_g = sc.rowstart[t.s][g + 1] - sc.rowstart[t.s][g];
   t.bn = sg.bn;
-  const int ks = local % sg.ksplit;  // K slice, fastest
-  local /= sg.ksplit;
-  const int ntb = (rows_g + t.bn - 1) / t.bn;
-  const int tr = sc.trows[t.s][lo];
-  t.mb = local / ntb;
-  t.tb = local - t.mb * ntb;
-  t.a_row = lo * sg.nout + t.mb * a.munit;
-  t.b_row = sc.rowstart[t.s][lo] + t.tb * tr;
+  int ks = 0;  // K slice, fastest
+  if (sg.ksplit > 1) {
+    ks = local % sg.ksplit;
+    local /= sg.ksplit;
+  }
+  const int packed = sc.trows[t.s][g];
+  const int tr = packed & 1023, ntb = packed >> 10;
+  if (ntb == 1) {
+    t.mb = local;
+    t.tb = 0;
+  } else {
+    t.mb = local / ntb;
+    t.tb = local - t.mb * ntb;
+  }
+  t.a_row = g * sg.nout + t.mb * a.munit;
+  t.b_row = sc.rowstart[t.s][g] + t.tb * tr;
   t.valid = min(tr, rows_g - t.tb * tr);
-  const int KB = sg.K / (kTileK * a.kps);  // stages of kps K blocks
-  t.kb0 = ks * KB / sg.ksplit;
-  t.kb1 = (ks + 1) * KB / sg.ksplit;
+  const int KB = sg.kstages;
+  if (sg.ksplit > 1) {
+    t.kb0 = ks * KB / sg.ksplit;
+    t.kb1 = (ks + 1) * KB / sg.ksplit;
+  } else {
+    t.kb0 = 0;
+    t.kb1 = KB;
+  }
   t.out_off = static_cast<size_t>(ks) * sg.slice_stride;
   return t;
 }
@@ -217,7 +237,8 @@ __device__ void build_schedule(const GemmArgs& a, Sched& sc) {
       // in step instead of a short last tile racing ahead.
       const int ntb = (rows_g + sg.bn - 1) / sg.bn;
       const int tiles = (g < sg.groups) ? mblocks * ntb * sg.ksplit : 0;
-      if (g < sg.groups) sc.trows[s][g] = ntb > 0 ? ((rows_g + ntb - 1) / ntb + 15) / 16 * 16 : sg.bn;
+      if (g < sg.groups)
+        sc.trows[s][g] = (ntb > 0 ? ((rows_g + ntb - 1) / ntb + 15) / 16 * 16 : sg.bn) | (max(ntb, 1) << 10);
       int incl = tiles;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -322,8 +343,9 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
       bool ok = true;
       int ps = 0;        // ring slot of stage `it` (it % S, kept as a running counter:
       uint32_t pph = 0;  // a division per stage is not free on the issue path) and its phase
+      WalkHint hint{0, 0};
       for (int tile = first; tile < total && ok; tile += stride) {
-        const Tile t = decode_tile(a, sc, tile);
+        const Tile t = decode_tile(a, sc, tile, hint);
         const SegMaps& ms = maps.seg[t.s];
         const bool two_maps = SWIGLU && a.seg[t.s].a_mode == kTwoMaps;  // then KPS == 1
         const int n_tile = MOE_EXACT_N ? ((t.valid + 15) >> 4) << 4 : t.bn;
@@ -423,8 +445,9 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
       int ms_ = 0;       // ring slot and phase of the next stage (running counters)
       uint32_t mph = 0;
       bool ok = true;
+      WalkHint hint{0, 0};
       for (int tile = first; tile < total && ok; tile += stride, ++n) {
-        const Tile t = decode_tile(a, sc, tile);
+        const Tile t = decode_tile(a, sc, tile, hint);
         const int acc = a.nslots == 2 ? (n & 1) : 0;
         const uint32_t aph = (a.nslots == 2 ? (n >> 1) : n) & 1;
         if (!mbar_wait(&tempty[acc], aph ^ 1, a.err, kSiteGemmMma)) break;
@@ -487,8 +510,9 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
     uint32_t xseq = 0;  // exchange chunk counter (the same sequence in both warps of a pair)
     bool ok = true;
     int n = 0;
+    WalkHint hint{0, 0};
     for (int tile = first; tile < total && ok; tile += stride, ++n) {
-      const Tile t = decode_tile(a, sc, tile);
+      const Tile t = decode_tile(a, sc, tile, hint);
       const int acc = a.nslots == 2 ? (n & 1) : 0;
       const uint32_t aph = (a.nslots == 2 ? (n >> 1) : n) & 1;
       if (!mbar_wait(&tfull[acc], aph, a.err, kSiteGemmEpilogue)) break;
@@ -826,7 +850,7 @@ cudaError_t launch_grouped_gemm(GemmEpilogue epi, int num_segments, const GemmSe
     const GemmSegment& g = segs[s];
     const int ks = (!k_splittable(epi) || g.ksplit < 1) ? 1 : g.ksplit;
     a.seg[s] = SegDev{g.offsets, g.groups, g.rows, g.nout, g.K, g.bn, g.ldo, ks, g.a_mode, g.up_first, g.gelu,
-                      g.slice_stride, g.out};
+                      g.slice_stride, g.out, g.K / (kTileK * plan.kps)};
     a.bn_max = a.bn_max > g.bn ? a.bn_max : g.bn;
     upper += static_cast<long long>(g.nout / a.munit) * ((g.rows + g.bn - 1) / g.bn + g.groups) * ks;
   }
