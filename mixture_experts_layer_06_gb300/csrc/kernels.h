@@ -102,7 +102,8 @@ int router_launches(int T, int H, int E, bool shared_gate);
 
 // Decode-sized batches: routing and the permutation (counts, offsets, perm,
 // inv, x_perm) in one single-CTA launch on the CUDA cores, when
-// route_permute_is_tiny (T <= 8 and E * H <= 128K router weights).
+// route_permute_is_tiny (T <= 8, E * H <= 128K router weights and T * H <=
+// 48K: the batch's x rows fit the kernel's shared memory).
 bool route_permute_is_tiny(int T, int H, int E, int k);
 cudaError_t launch_route_permute_tiny(int T, int H, int E, int k, const RouteSpec& spec, const void* x,
                                       const void* w_router, const void* w_shared_gate, int32_t* topk_idx,

@@ -663,10 +663,12 @@ __global__ void shared_gate_kernel(const __nv_bfloat16* __restrict__ x, const __
 }
 
 // Decode-sized batches (T <= kTinyT, router weights of at most kTinyWr
-// elements): routing and the grouping onto experts in one CTA, one launch.
-//  1. logits[t][e] = x[t] . W_r[e] (and x[t] . w_s for a gated shared
-//     expert): one warp per (token, expert) pair on the CUDA cores, fp32
-//     accumulation of the bf16 products, 16-byte loads;
+// elements, x of at most kTinyX): routing and the grouping onto experts in
+// one CTA, one launch.
+//  1. the T rows of x into shared memory; logits[t][e] = x[t] . W_r[e] (and
+//     x[t] . w_s for a gated shared expert): one warp per (token, column)
+//     pair on the CUDA cores, fp32 accumulation of the bf16 products,
+//     16-byte loads;
 //  2. score, group limit and top-k by the same 8-lane team routine as
 //     router_kernel;
 //  3. counts, offsets (exclusive scan) and, for copy q = t*k + j of expert e,
@@ -674,7 +676,8 @@ __global__ void shared_gate_kernel(const __nv_bfloat16* __restrict__ x, const __
 //  4. perm, inv, and the x rows copied to x_perm.
 constexpr int kTinyT = 8;
 constexpr int kTinyWr = 128 * 1024;  // E * H
-constexpr int kTinyThreads = 256;
+constexpr int kTinyX = 48 * 1024;    // T * H: the batch's x rows, staged in shared memory (96 KB at most)
+constexpr int kTinyThreads = 512;
 
 struct TinyArgs {
   RouterArgs r;
@@ -685,20 +688,38 @@ struct TinyArgs {
   uint4* x_perm;
 };
 
-__device__ __forceinline__ float dot_bf16_row(const __nv_bfloat16* a, const __nv_bfloat16* b, int H, int lane) {
-  const uint4* av = reinterpret_cast<const uint4*>(a);
-  const uint4* bv = reinterpret_cast<const uint4*>(b);
-  float acc = 0.f;
-  for (int v = lane; v < H / 8; v += 32) {
-    const uint4 xa = av[v], wa = bv[v];
-    const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&xa);
-    const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wa);
+// fp32 sum of the products of 8 bf16 pairs (one 16-byte load of each), into acc.
+__device__ __forceinline__ void fma8_bf16(const uint4& xa, const uint4& wa, float& acc) {
+  const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&xa);
+  const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(&wa);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 xf = __bfloat1622float2(xp[i]), wf = __bfloat1622float2(wp[i]);
-      acc = fmaf(xf.x, wf.x, acc);
-      acc = fmaf(xf.y, wf.y, acc);
-    }
+  for (int i = 0; i < 4; ++i) {
+    const float2 xf = __bfloat1622float2(xp[i]), wf = __bfloat1622float2(wp[i]);
+    acc = fmaf(xf.x, wf.x, acc);
+    acc = fmaf(xf.y, wf.y, acc);
+  }
+}
+
+// xs . w over H bf16 values (xs: one token's row in shared memory, H/8
+// 16-byte vectors) by one warp (H a multiple of 8), fp32; the sum ends up in
+// every lane.  A short loop with four weight loads in flight per lane: this
+// one-CTA kernel runs once per forward from a cold instruction cache, and
+// unrolling further measured slower (Mixtral-shaped T=1, logits of 8
+// experts: 4 loads in flight 12 us, 8 loads 19 us, 16 loads 32 us when the
+// loop also covered every token).
+__device__ __noinline__ float dot_row_tiny(const uint4* xs, const __nv_bfloat16* w, int H, int lane) {
+  constexpr int kU = 4;
+  const uint4* wv = reinterpret_cast<const uint4*>(w);
+  const int n = H / 8;
+  float acc = 0.f;
+  for (int v0 = lane; v0 < n; v0 += 32 * kU) {
+    uint4 wa[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (v0 + 32 * u < n) wa[u] = wv[v0 + 32 * u];
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (v0 + 32 * u < n) fma8_bf16(xs[v0 + 32 * u], wa[u], acc);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
@@ -710,16 +731,35 @@ __global__ void __launch_bounds__(kTinyThreads, 1) route_permute_tiny_kernel(con
   __shared__ float bias_s[256];
   __shared__ int32_t idx_s[kTinyT * 16];
   __shared__ int32_t off_s[257];
+  __shared__ int32_t row_s[kTinyT * 16];  // grouped row of copy q
+  extern __shared__ uint4 x_s[];          // the batch's x rows, T x H/8 vectors
   pdl_trigger();
   pdl_wait();
   const RouterArgs& a = ta.r;
   const int T = a.T, E = a.E, k = a.k, H = a.H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ncol = E + (ta.w_shared_gate != nullptr ? 1 : 0);  // the gate is column E
+  const int H8 = H / 8;
+  {
+    // x into shared memory, four loads in flight per thread
+    const uint4* xg = reinterpret_cast<const uint4*>(ta.x);
+    const int total = T * H8;
+    for (int i0 = threadIdx.x; i0 < total; i0 += 4 * kTinyThreads) {
+      uint4 val[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i0 + u * kTinyThreads < total) val[u] = xg[i0 + u * kTinyThreads];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i0 + u * kTinyThreads < total) x_s[i0 + u * kTinyThreads] = val[u];
+    }
+  }
+  __syncthreads();
+  // One warp per (token, column) pair, x from shared memory.
   for (int p = warp; p < T * ncol; p += kTinyThreads / 32) {
     const int t = p / ncol, e = p - t * ncol;
     const __nv_bfloat16* w = e < E ? ta.w_router + static_cast<size_t>(e) * H : ta.w_shared_gate;
-    const float v = dot_bf16_row(ta.x + static_cast<size_t>(t) * H, w, H, lane);
+    const float v = dot_row_tiny(x_s + t * H8, w, H, lane);
     if (lane == 0) logits[e * kTinyT + t] = v;
   }
   if (a.spec.logit_bias != nullptr)
@@ -767,21 +807,14 @@ __global__ void __launch_bounds__(kTinyThreads, 1) route_permute_tiny_kernel(con
     const int r = row_of(q);
     ta.perm[r] = q;
     ta.inv[q] = r;
+    row_s[q] = r;
   }
-  const int H8 = H / 8;
-  for (int q = 0; q < T * k; ++q) {
-    const int r = row_of(q);  // the same for every thread
-    const uint4* src = reinterpret_cast<const uint4*>(ta.x + static_cast<size_t>(q / k) * H);
-    uint4* dst = ta.x_perm + static_cast<size_t>(r) * H8;
-    for (int v0 = threadIdx.x; v0 < H8; v0 += 4 * kTinyThreads) {
-      uint4 val[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (v0 + u * kTinyThreads < H8) val[u] = src[v0 + u * kTinyThreads];
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (v0 + u * kTinyThreads < H8) dst[v0 + u * kTinyThreads] = val[u];
-    }
+  __syncthreads();
+  // x_perm: the T*k copies of the staged rows
+  const int total = T * k * H8;
+  for (int i = threadIdx.x; i < total; i += kTinyThreads) {
+    const int q = i / H8, v = i - q * H8;
+    ta.x_perm[static_cast<size_t>(row_s[q]) * H8 + v] = x_s[(q / k) * H8 + v];
   }
 }
 
@@ -816,7 +849,8 @@ RouterPlan router_plan(int T, int H, int E, bool shared_gate) {
 }
 
 bool route_permute_is_tiny(int T, int H, int E, int k) {
-  return T >= 1 && T <= kTinyT && static_cast<long long>(E) * H <= kTinyWr && E <= 256 && k <= 16;
+  return T >= 1 && T <= kTinyT && static_cast<long long>(E) * H <= kTinyWr && T * H <= kTinyX && E <= 256 &&
+         k <= 16;
 }
 
 cudaError_t launch_route_permute_tiny(int T, int H, int E, int k, const RouteSpec& spec, const void* x,
@@ -842,7 +876,17 @@ cudaError_t launch_route_permute_tiny(int T, int H, int E, int k, const RouteSpe
   t.perm = perm;
   t.inv = inv;
   t.x_perm = static_cast<uint4*>(x_perm);
-  return launch_kernel(route_permute_tiny_kernel, dim3(1), dim3(kTinyThreads), 0, stream, t);
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !configured[dev]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(route_permute_tiny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTinyX * 2);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const size_t smem = static_cast<size_t>(T) * H * 2;  // the staged x rows
+  return launch_kernel(route_permute_tiny_kernel, dim3(1), dim3(kTinyThreads), smem, stream, t);
 }
 
 int router_launches(int T, int H, int E, bool shared_gate) {
