@@ -42,6 +42,12 @@ namespace {
 #define MOE_EXACT_N 1
 #endif
 
+// L2 cache policies on the TMA loads: weights evict-first, token rows
+// evict-last (0: both normal).
+#ifndef MOE_L2_HINTS
+#define MOE_L2_HINTS 1
+#endif
+
 
 constexpr int kThreads = 192;
 constexpr int kMaxStages = 8;
@@ -136,6 +142,7 @@ __device__ __forceinline__ int box_index(const SegMaps& ms, int rows_per_cta) {
 
 struct Tile {
   int s, g, mb, tb, a_row, b_row, valid, bn, kb0, kb1;
+  int ntb;  // token tiles of the group (each streams the same weight tiles)
   size_t out_off;  // element offset of this tile's output slice
 };
 
@@ -189,6 +196,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const Sched& sc, 
   }
   const int packed = sc.trows[t.s][g];
   const int tr = packed & 1023, ntb = packed >> 10;
+  t.ntb = ntb;
   if (ntb == 1) {
     t.mb = local;
     t.tb = 0;
@@ -340,6 +348,12 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
         if (SWIGLU && a.seg[sg].a_mode == kTwoMaps) tma_prefetch_map(&maps.seg[sg].a1);
         for (int i = 0; i < maps.seg[sg].nb; ++i) tma_prefetch_map(&maps.seg[sg].b[i]);
       }
+      // L2 policies: token rows are re-read by every weight block of their
+      // group (evict last); a weight tile read by one token tile only is
+      // streamed (evict first), one shared by several stays normal.
+      const uint64_t p_first = MOE_L2_HINTS ? l2_policy_evict_first() : l2_policy_evict_normal();
+      const uint64_t p_normal = l2_policy_evict_normal();
+      const uint64_t pb = MOE_L2_HINTS ? l2_policy_evict_last() : l2_policy_evict_normal();
       bool ok = true;
       int ps = 0;        // ring slot of stage `it` (it % S, kept as a running counter:
       uint32_t pph = 0;  // a division per stage is not free on the issue path) and its phase
@@ -354,6 +368,7 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
         // the smallest token box that covers this CTA's n_tile / BDIV rows
         const int bi = box_index(ms, n_tile / BDIV);
         const CUtensorMap* mb = &ms.b[bi];
+        const uint64_t pa = t.ntb == 1 ? p_first : p_normal;
         const uint32_t bytes = BDIV * KPS * (NSUB * kATileBytes + (bi + 1) * ms.bstep * kTileK * 2);
         for (int kb = t.kb0; kb < t.kb1; ++kb, ++it) {
           const int s = ps;
@@ -373,58 +388,60 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
             const uint32_t bar = mapa_shared(smem_u32(&full[s]), 0);
             if (two_maps) {
               for (int u = 0; u < NSUB; ++u) {
-                tma_load_2d_pair(st + u * kATileBytes, &ms.a0, bar, kb * kTileK, a_row + u * kHalfRows);
-                tma_load_2d_pair(st + u * kATileBytes + kHalfBytes, &ms.a1, bar, kb * kTileK, a_row + u * kHalfRows);
+                tma_load_2d_pair_hint(st + u * kATileBytes, &ms.a0, bar, kb * kTileK, a_row + u * kHalfRows, pa);
+                tma_load_2d_pair_hint(st + u * kATileBytes + kHalfBytes, &ms.a1, bar, kb * kTileK,
+                                      a_row + u * kHalfRows, pa);
               }
             } else if (SWIGLU) {
               for (int u = 0; u < NSUB; ++u) {  // sub-tile u: its KPS A tiles, KPS * 16 KB
                 uint8_t* dst = st + u * KPS * kATileBytes;
                 if (KPS == 1)
-                  tma_load_3d_pair(dst, &ms.a0, bar, kb * kTileK, a_row + u * kHalfRows, 0);
+                  tma_load_3d_pair_hint(dst, &ms.a0, bar, kb * kTileK, a_row + u * kHalfRows, 0, pa);
                 else
-                  tma_load_4d_pair(dst, &ms.a0, bar, 0, a_row + u * kHalfRows, 0, kb * KPS);
+                  tma_load_4d_pair_hint(dst, &ms.a0, bar, 0, a_row + u * kHalfRows, 0, kb * KPS, pa);
               }
             } else {
               for (int u = 0; u < NSUB; ++u) {  // sub-tile u: 128 weight rows, KPS * 16 KB
                 uint8_t* dst = st + u * KPS * kATileBytes;
                 if (KPS == 1)
-                  tma_load_2d_pair(dst, &ms.a0, bar, kb * kTileK, a_row + u * kTileM);
+                  tma_load_2d_pair_hint(dst, &ms.a0, bar, kb * kTileK, a_row + u * kTileM, pa);
                 else
-                  tma_load_3d_pair(dst, &ms.a0, bar, 0, a_row + u * kTileM, kb * KPS);
+                  tma_load_3d_pair_hint(dst, &ms.a0, bar, 0, a_row + u * kTileM, kb * KPS, pa);
               }
             }
             if (KPS == 1)
-              tma_load_2d_pair(sb, mb, bar, kb * kTileK, b_row);
+              tma_load_2d_pair_hint(sb, mb, bar, kb * kTileK, b_row, pb);
             else
-              tma_load_3d_pair(sb, mb, bar, 0, b_row, kb * KPS);
+              tma_load_3d_pair_hint(sb, mb, bar, 0, b_row, kb * KPS, pb);
           } else {
             mbar_arrive_expect_tx(&full[s], bytes);
             if (two_maps) {
               for (int u = 0; u < NSUB; ++u) {
-                tma_load_2d(st + u * kATileBytes, &ms.a0, &full[s], kb * kTileK, a_row + u * kHalfRows);
-                tma_load_2d(st + u * kATileBytes + kHalfBytes, &ms.a1, &full[s], kb * kTileK, a_row + u * kHalfRows);
+                tma_load_2d_hint(st + u * kATileBytes, &ms.a0, &full[s], kb * kTileK, a_row + u * kHalfRows, pa);
+                tma_load_2d_hint(st + u * kATileBytes + kHalfBytes, &ms.a1, &full[s], kb * kTileK,
+                                 a_row + u * kHalfRows, pa);
               }
             } else if (SWIGLU) {
               for (int u = 0; u < NSUB; ++u) {
                 uint8_t* dst = st + u * KPS * kATileBytes;
                 if (KPS == 1)
-                  tma_load_3d(dst, &ms.a0, &full[s], kb * kTileK, a_row + u * kHalfRows, 0);
+                  tma_load_3d_hint(dst, &ms.a0, &full[s], kb * kTileK, a_row + u * kHalfRows, 0, pa);
                 else
-                  tma_load_4d(dst, &ms.a0, &full[s], 0, a_row + u * kHalfRows, 0, kb * KPS);
+                  tma_load_4d_hint(dst, &ms.a0, &full[s], 0, a_row + u * kHalfRows, 0, kb * KPS, pa);
               }
             } else {
               for (int u = 0; u < NSUB; ++u) {
                 uint8_t* dst = st + u * KPS * kATileBytes;
                 if (KPS == 1)
-                  tma_load_2d(dst, &ms.a0, &full[s], kb * kTileK, a_row + u * kTileM);
+                  tma_load_2d_hint(dst, &ms.a0, &full[s], kb * kTileK, a_row + u * kTileM, pa);
                 else
-                  tma_load_3d(dst, &ms.a0, &full[s], 0, a_row + u * kTileM, kb * KPS);
+                  tma_load_3d_hint(dst, &ms.a0, &full[s], 0, a_row + u * kTileM, kb * KPS, pa);
               }
             }
             if (KPS == 1)
-              tma_load_2d(sb, mb, &full[s], kb * kTileK, b_row);
+              tma_load_2d_hint(sb, mb, &full[s], kb * kTileK, b_row, pb);
             else
-              tma_load_3d(sb, mb, &full[s], 0, b_row, kb * KPS);
+              tma_load_3d_hint(sb, mb, &full[s], 0, b_row, kb * KPS, pb);
           }
         }
       }
