@@ -32,8 +32,9 @@ namespace {
 
 // warp 0: TMA, warp 1: MMA + TMEM owner, warps 2-9: TMEM -> shared memory
 // (two column halves per TMEM lane quadrant); every warp takes part in the
-// reduction and the selection (48 teams of 8 lanes).
-constexpr int kThreads = 384;
+// reduction and the selection (64 teams of 8 lanes: the 64 tokens a CTA owns
+// at a 2-way K split take one pass).
+constexpr int kThreads = 512;
 constexpr int kEpiWarps = 8;
 constexpr int kMaxStages = 8;
 constexpr int kMaxCluster = 8;
@@ -615,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = threadIdx.x; e < a.E; e += kThreads) bias_s[e] = a.spec.logit_bias[e];
     __syncthreads();
   }
-  // Selection: team i of 8 lanes takes owned rows i, i + 24, ...
+  // Selection: team i of 8 lanes takes owned rows i, i + kTeams, ...
   constexpr int kTeams = kThreads / kTeam;
   const int team = threadIdx.x / kTeam, tl = threadIdx.x % kTeam;
   for (int base = 0; base < rpc; base += kTeams) {
