@@ -30,12 +30,11 @@
 namespace moe {
 namespace {
 
-// warp 0: TMA, warp 1: MMA + TMEM owner, warps 2-9: TMEM -> shared memory
-// (two column halves per TMEM lane quadrant); every warp takes part in the
-// reduction and the selection (64 teams of 8 lanes: the 64 tokens a CTA owns
-// at a 2-way K split take one pass).
+// warp 0: TMA, warp 1: MMA + TMEM owner; then every warp takes part in the
+// TMEM -> shared memory exchange (warp w: TMEM lane quadrant w % 4, column
+// part w / 4), the reduction and the selection (64 teams of 8 lanes: the 64
+// tokens a CTA owns at a 2-way K split take one pass).
 constexpr int kThreads = 512;
-constexpr int kEpiWarps = 8;
 constexpr int kMaxStages = 8;
 constexpr int kMaxCluster = 8;
 constexpr int kPairMinT = 4096;  // batches from which the router runs as CTA pairs (router_plan)
@@ -531,16 +530,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // Every CTA of the cluster reaches every cluster barrier, whatever happened
   // above (a wait that gave up has recorded the error and the role stopped).
-  // Barrier 1: every MMA of the cluster has completed (the epilogue warps
-  // waited for their own accumulator), so every CTA's pipeline stages are free
-  // to receive partial logits.
-  bool acc_ok = true;
-  const bool epi = warp >= 2 && warp < 2 + kEpiWarps;
-  if (epi) {
-    acc_ok = mbar_wait(acc_full, 0, a.err, kSiteRouterEpilogue);
-    acc_ok = __all_sync(0xFFFFFFFFu, acc_ok);  // the TMEM loads below are warp-collective
-    tc_fence_after_sync();
-  }
+  // Barrier 1: every MMA of the cluster has completed (every warp waited for
+  // its own accumulator), so every CTA's pipeline stages are free to receive
+  // partial logits.
+  bool acc_ok = mbar_wait(acc_full, 0, a.err, kSiteRouterEpilogue);
+  acc_ok = __all_sync(0xFFFFFFFFu, acc_ok);  // the TMEM loads below are warp-collective
+  tc_fence_after_sync();
   __syncthreads();
   if (CL > 1) cluster_sync();
 
@@ -550,14 +545,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rpc = kTileM / static_cast<int>(C);
   const int ld = logit_ld(static_cast<int>(C));
   const int slot_floats = a.NE * ld;
-  // Column halves: warps 2-5 take columns [0, NE/2), warps 6-9 [NE/2, NE)
-  // (NE a multiple of 64), else warps 2-5 take all columns.
-  const int halves = a.NE % 64 == 0 ? 2 : 1;
-  const int half = (warp - 2) / 4;
-  if (epi && acc_ok && half < halves) {
+  // Column parts: NE split into 4 (NE a multiple of 128), 2 (of 64) or 1;
+  // warp w takes part w / 4 of its lane quadrant's columns.
+  const int parts = a.NE % 128 == 0 ? 4 : a.NE % 64 == 0 ? 2 : 1;
+  const int part = warp >> 2;
+  if (acc_ok && part < parts) {
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    const int cbeg = half * (a.NE / halves), cend = cbeg + a.NE / halves;
+    const int cbeg = part * (a.NE / parts), cend = cbeg + a.NE / parts;
     const uint32_t owner = static_cast<uint32_t>(row / rpc);  // its K share index
     const int rr = row - static_cast<int>(owner) * rpc;  // row within the owner's share
     float* slot = P + static_cast<size_t>(kr) * slot_floats;
