@@ -662,9 +662,9 @@ __global__ void shared_gate_kernel(const __nv_bfloat16* __restrict__ x, const __
 // elements, x of at most kTinyX): routing and the grouping onto experts in
 // one CTA, one launch.
 //  1. the T rows of x into shared memory; logits[t][e] = x[t] . W_r[e] (and
-//     x[t] . w_s for a gated shared expert): one warp per (token, column)
-//     pair on the CUDA cores, fp32 accumulation of the bf16 products,
-//     16-byte loads;
+//     x[t] . w_s for a gated shared expert): one warp per column, each
+//     weight row read once, on the CUDA cores, fp32 accumulation of the
+//     bf16 products, 16-byte loads;
 //  2. score, group limit and top-k by the same 8-lane team routine as
 //     router_kernel;
 //  3. counts, offsets (exclusive scan) and, for copy q = t*k + j of expert e,
@@ -696,30 +696,39 @@ __device__ __forceinline__ void fma8_bf16(const uint4& xa, const uint4& wa, floa
   }
 }
 
-// xs . w over H bf16 values (xs: one token's row in shared memory, H/8
-// 16-byte vectors) by one warp (H a multiple of 8), fp32; the sum ends up in
-// every lane.  A short loop with four weight loads in flight per lane: this
+// out[t] = xs[t] . w for the T token rows in shared memory (xs: T rows of
+// H/8 16-byte vectors), by one warp (H a multiple of 8), fp32.  The weight row
+// is read once, in chunks of 8 vectors per lane held in registers while a
+// runtime loop over the tokens adds each token's partial dot product (warp
+// reduction, lane 0 accumulates into out).  The code stays short: this
 // one-CTA kernel runs once per forward from a cold instruction cache, and
-// unrolling further measured slower (Mixtral-shaped T=1, logits of 8
-// experts: 4 loads in flight 12 us, 8 loads 19 us, 16 loads 32 us when the
-// loop also covered every token).
-__device__ __noinline__ float dot_row_tiny(const uint4* xs, const __nv_bfloat16* w, int H, int lane) {
-  constexpr int kU = 4;
+// fully unrolled variants measured slower (Mixtral-shaped T=1, logits of 8
+// experts: 12 / 19 / 32 us with 4 / 8 / 16 loads in flight when the loop was
+// also unrolled over every token, 5 us with one load at a time).
+__device__ __noinline__ void column_tiny(const uint4* xs, const __nv_bfloat16* w, int T, int H, int lane,
+                                         float* out) {
+  constexpr int kU = 8;
   const uint4* wv = reinterpret_cast<const uint4*>(w);
   const int n = H / 8;
-  float acc = 0.f;
-  for (int v0 = lane; v0 < n; v0 += 32 * kU) {
+  if (lane < T) out[lane] = 0.f;
+  __syncwarp();
+  for (int c0 = 0; c0 < n; c0 += 32 * kU) {
+    const int v0 = c0 + lane;
     uint4 wa[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u)
       if (v0 + 32 * u < n) wa[u] = wv[v0 + 32 * u];
+    for (int t = 0; t < T; ++t) {
+      float acc = 0.f;
 #pragma unroll
-    for (int u = 0; u < kU; ++u)
-      if (v0 + 32 * u < n) fma8_bf16(xs[v0 + 32 * u], wa[u], acc);
+      for (int u = 0; u < kU; ++u)
+        if (v0 + 32 * u < n) fma8_bf16(xs[t * n + v0 + 32 * u], wa[u], acc);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+      if (lane == 0) out[t] += acc;
+    }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-  return acc;
+  __syncwarp();
 }
 
 __global__ void __launch_bounds__(kTinyThreads, 1) route_permute_tiny_kernel(const TinyArgs ta) {
@@ -751,12 +760,10 @@ __global__ void __launch_bounds__(kTinyThreads, 1) route_permute_tiny_kernel(con
     }
   }
   __syncthreads();
-  // One warp per (token, column) pair, x from shared memory.
-  for (int p = warp; p < T * ncol; p += kTinyThreads / 32) {
-    const int t = p / ncol, e = p - t * ncol;
+  // One warp per column, against every token's x from shared memory.
+  for (int e = warp; e < ncol; e += kTinyThreads / 32) {
     const __nv_bfloat16* w = e < E ? ta.w_router + static_cast<size_t>(e) * H : ta.w_shared_gate;
-    const float v = dot_row_tiny(x_s + t * H8, w, H, lane);
-    if (lane == 0) logits[e * kTinyT + t] = v;
+    column_tiny(x_s, w, T, H, lane, logits + e * kTinyT);
   }
   if (a.spec.logit_bias != nullptr)
     for (int e = threadIdx.x; e < E; e += kTinyThreads) bias_s[e] = a.spec.logit_bias[e];
