@@ -225,11 +225,17 @@ moe::RouteSpec route_spec(const moe_config_t& c) {
 // against the mean-sized box: Mixtral-shaped T=128 600 -> 482 us, T=512
 // 598 -> 535 us; Qwen2-shaped T=512 891 -> 827 us; DeepSeek-V3-shaped T=2048
 // 4152 -> 3844 us; skew T=512 alpha=0 268 -> 242 us, alpha=2 235 -> 172 us.
-// A box of four times the mean helps heavy skew further but is slower on the
-// DeepSeek-V3-shaped layer.  A single group (dense or shared expert) keeps
-// the exact box.
+// A box of four times the mean helps heavy skew further but is slower where
+// it moves the layer onto CTA pairs (Qwen2-shaped T=512, DeepSeek-V3-shaped
+// T=2048) or where experts get a handful of rows (Mixtral-shaped T=32).  So
+// experts averaging 32..63 rows take 4x (a 128-row box, still a single-CTA
+// plan): skew T=512 alpha=2 (hot experts of ~500 rows) then runs half as many
+// tiles.  A single group (dense or shared expert) keeps the exact box.
 #ifndef MOE_BOX_SCALE
 #define MOE_BOX_SCALE 2
+#endif
+#ifndef MOE_BOX_WIDE
+#define MOE_BOX_WIDE 1
 #endif
 #ifndef MOE_BOX_MIN_GROUPS
 #define MOE_BOX_MIN_GROUPS 2
@@ -241,8 +247,10 @@ int choose_bn(long long rows, int groups, int bn_max = 256) {
   const long long avg = (rows + groups - 1) / (groups > 0 ? groups : 1);
   int bn = 16;
   while (bn < bn_max && bn < avg) bn <<= 1;
-  if (groups >= MOE_BOX_MIN_GROUPS)
+  if (groups >= MOE_BOX_MIN_GROUPS) {
     for (int i = 1; i < MOE_BOX_SCALE && bn < bn_max; i <<= 1) bn <<= 1;
+    if (MOE_BOX_WIDE && bn == 64 && avg >= 32 && bn_max >= 128) bn = 128;
+  }
   return bn;
 }
 
