@@ -166,6 +166,8 @@ __global__ void gather_kernel(const int32_t* __restrict__ idx, const uint4* __re
 // Same arithmetic, same results as the three-launch form.
 constexpr int kSmallT = 512;
 constexpr int kSmallThreads = 256;
+constexpr int kSmallIdx = 2048;  // most copies (T * k) a one-launch permute takes
+constexpr int kSmallMaxK = 16;   // most experts per token
 
 __global__ void __launch_bounds__(kSmallThreads)
     permute_small_kernel(const int32_t* __restrict__ idx, const uint4* __restrict__ x, int T, int H8, int E, int k,
@@ -175,23 +177,30 @@ __global__ void __launch_bounds__(kSmallThreads)
   __shared__ uint32_t rowbase[kSmallT / 32][256];
   __shared__ int32_t off_s[257];
   __shared__ int32_t warp_tot[8];
+  __shared__ int32_t idx_s[kSmallIdx];  // the expert ids (-1: out of range), for the row lookups
   pdl_trigger();
   pdl_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int W = (T + 31) / 32;
   for (int i = tid; i < W * 256; i += kSmallThreads) bm[i / 256][i % 256] = 0;
   __syncthreads();
-  // bitmaps: warp w' handles token words w', w' + 8, ...
+  // bitmaps: warp w' handles token words w', w' + 8, ...; a token's k ids are
+  // loaded together (one round trip, not k)
   for (int w = warp; w < W; w += kSmallThreads / 32) {
     const int t = w * 32 + lane;
-    for (int j = 0; j < k; ++j) {
-      int e = -1;
+    int ev[kSmallMaxK];
+#pragma unroll
+    for (int j = 0; j < kSmallMaxK; ++j) ev[j] = (j < k && t < T) ? idx[static_cast<size_t>(t) * k + j] : -1;
+#pragma unroll
+    for (int j = 0; j < kSmallMaxK; ++j) {
+      if (j >= k) break;  // uniform
+      int e = ev[j];
       if (t < T) {
-        e = idx[static_cast<size_t>(t) * k + j];
         if (e < 0 || e >= E) {
           if (blockIdx.x == 0) raise_error(err, kErrBounds, kSitePermuteIndex);
           e = -1;
         }
+        idx_s[t * k + j] = e;
       }
       const uint32_t peers = __match_any_sync(0xFFFFFFFFu, e);
       if (e >= 0 && lane == __ffs(peers) - 1) {
@@ -233,8 +242,8 @@ __global__ void __launch_bounds__(kSmallThreads)
   const int rows = T * k;
   auto row_of = [&](int q) {
     const int t = q / k;
-    const int e = idx[q];
-    if (e < 0 || e >= E) return -1;
+    const int e = idx_s[q];
+    if (e < 0) return -1;
     const int r = static_cast<int>(rowbase[t >> 5][e] + __popc(bm[t >> 5][e] & ((1u << (t & 31)) - 1u)));
     return r < rows ? r : -1;
   };
@@ -270,6 +279,7 @@ __global__ void __launch_bounds__(kSmallThreads)
 // rows (Mixtral-shaped T=512: 10.5 vs 14 us) and loses above (4096 rows:
 // 29-35 vs 17-21 us).
 constexpr int kSmallRows = 2048;
+static_assert(kSmallRows <= kSmallIdx, "the one-launch permute keeps every copy's expert id in shared memory");
 
 bool permute_is_small(int T, int E, int k) { return T <= kSmallT && E <= 256 && T * k <= kSmallRows; }
 
