@@ -24,7 +24,9 @@
 //            epilogue warps that read the gate lanes and the up lanes of the
 //            same features trade half of each 32-column chunk through shared
 //            memory and each finishes h = SiLU(g) * u for its half -> bf16.
-//   Store:   128 output rows per CTA (down projection) -> fp32.
+//   Store:   128 output rows per CTA -> fp16 (the down projection's expert
+//            outputs, K-split slices at small batches), fp32, or bf16 (the
+//            unfused gate / up projections of the fusion ablation).
 // Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
 // owner, warps 2-5 epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
 // Pipelines: a ring of `stages` shared-memory slots (full/empty mbarriers) and
@@ -42,8 +44,9 @@ namespace {
 #define MOE_EXACT_N 1
 #endif
 
-// L2 cache policies on the TMA loads: weights evict-first, token rows
-// evict-last (0: both normal).
+// L2 cache policies on the TMA loads: token rows evict-last, a weight tile
+// read by a single token tile evict-first, other weight tiles normal (0: all
+// normal).
 #ifndef MOE_L2_HINTS
 #define MOE_L2_HINTS 1
 #endif
@@ -337,8 +340,9 @@ __device__ __forceinline__ void gemm_body(const GemmMaps& maps, const GemmArgs& 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     // One elected lane: wait for a free slot, post the byte count, issue the
-    // loads of the weight tile and of the token tile.  The token box is
-    // always bn rows (bn/2 per CTA of a pair; one request); rows past the
+    // loads of the weight tile and of the token tile.  The token rows come in
+    // one request per stage through the smallest of the segment's box heights
+    // that covers this CTA's share of the tile (box_index); rows past the
     // tile's own are not used.  Several smaller boxes per tile were measured
     // to be much slower.
     int it = 0;
