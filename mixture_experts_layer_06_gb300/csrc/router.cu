@@ -839,10 +839,17 @@ RouterPlan router_plan(int T, int H, int E, bool shared_gate) {
   // The largest power-of-two K split c (a cluster of c CTAs, or c pairs;
   // at most 8 CTAs) that keeps the grid within one wave of ~152 CTAs and
   // leaves every CTA at least two K blocks, so that the W_r stream of a small
-  // batch spreads over several SMs.  Shapes only.
+  // batch spreads over several SMs.  Unpaired, clusters of 8 only while the
+  // grid stays within half the SMs: measured on GB300, the DeepSeek-V3-shaped router at
+  // T=2048 (16 token tiles) takes 58 us in clusters of 8 (128 CTAs) and
+  // 38 us in clusters of 4, while at T=512 (4 tiles, 32 CTAs) 8 beats 4
+  // (34 vs 38 us), as it does for every smaller router measured (Mixtral-,
+  // Qwen2- and skew-shaped layers, T=32..512).  Shapes only.
   const int per = p.pair ? 2 : 1;
   int c = 1;
-  while (per * c < kMaxCluster && p.m_tiles * per * (2 * c) <= 152 && KB / (2 * c) >= 2) c <<= 1;
+  while (per * c < kMaxCluster && p.m_tiles * per * (2 * c) <= 152 && KB / (2 * c) >= 2 &&
+         !(per == 1 && 2 * c >= kMaxCluster && p.m_tiles * (2 * c) > 76))
+    c <<= 1;
   p.kb_per_cta = (KB + c - 1) / c;
   while (c > 1 && (c - 1) * p.kb_per_cta >= KB) c >>= 1;  // every CTA gets a K block
   p.kb_per_cta = (KB + c - 1) / c;
