@@ -33,6 +33,9 @@ ROUTER_CASES = [
     ("qwen2", 256, {}),
     ("skew", 256, {"alpha": 0.0}), ("skew", 512, {"alpha": 1.0}), ("skew", 512, {"alpha": 2.0}),
     ("deepseek", 512, {}),
+    # unpaired batches of 10+ token tiles, whose K split stops at clusters of 4
+    # (the grid would pass half the SMs with clusters of 8)
+    ("deepseek", 2048, {}), ("mixtral", 2000, {}),
     # group-limited variants: 8 groups of 8 (groups inside a 32-column block),
     # top-3 / top-1 per group, 16 groups of 16
     ("deepseek", 256, {"E": 64}), ("deepseek", 256, {"group_topn": 3}), ("deepseek", 256, {"group_topn": 1}),
